@@ -1,0 +1,183 @@
+// C ABI of libfp8fg.so (declared in include/fp8fg.h): host-side argument validation,
+// device capability checks, per-thread error messages and the device status word.
+// No entry point allocates or frees memory.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/fp8fg.h"
+#include "internal.h"
+
+namespace fp8fg {
+cudaError_t read_and_clear_status(unsigned* out);
+}
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+  return fail(FP8FG_ERR_CUDA, "%s failed: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int supported = 0;
+  int known = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+// Looks up (once per device) the SM count and whether the current device is an
+// sm_103 GPU, the only architecture this library is built for.
+int current_device(DeviceInfo* out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FP8FG_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_devices_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if ((err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+      return cuda_fail(err, "cudaDeviceGetAttribute");
+    }
+    d.sm_count = sms;
+    d.supported = (major == 10 && minor == 3);
+    d.known = 1;
+  }
+  if (!d.supported) return fail(FP8FG_ERR_UNSUPPORTED, "device %d is not an sm_103 (B300) GPU", dev);
+  *out = d;
+  return FP8FG_OK;
+}
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8fg_last_error(void) { return g_last_error; }
+
+int fp8fg_version(void) { return 100; }
+
+int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, int transposed, uint8_t* q, float* s,
+                        fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (M < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: negative size M=%lld K=%lld", (long long)M, (long long)K);
+  if (transposed != 0 && transposed != 1) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: transposed must be 0 or 1");
+  if (ldx < K) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: ldx=%lld < K=%lld", (long long)ldx, (long long)K);
+  if (ldx % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: ldx must be a multiple of 8 elements");
+  if (transposed == 0 && K % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: K=%lld is not a multiple of 128", (long long)K);
+  if (transposed == 1 && M % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128 (transposed): M=%lld is not a multiple of 128", (long long)M);
+  if (transposed == 1 && K % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128 (transposed): K=%lld is not a multiple of 8", (long long)K);
+  if (M > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: dimension too large");
+  if (M == 0 || K == 0) return FP8FG_OK;
+  if (!x || !q || !s) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: null pointer");
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128: pointers must be 16-byte aligned");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err = transposed
+                        ? fp8fg::launch_quant_act_cols(x, M, K, ldx, q, s, reinterpret_cast<cudaStream_t>(stream))
+                        : fp8fg::launch_quant_act_rows(x, M, K, ldx, q, s, reinterpret_cast<cudaStream_t>(stream),
+                                                       dev.sm_count);
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_act_1x128 launch");
+  return FP8FG_OK;
+}
+
+int fp8_quant_w_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
+                        fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: negative size");
+  if (N % 128 || K % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: N=%lld and K=%lld must be multiples of 128", (long long)N, (long long)K);
+  if (ldw < K || ldw % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: ldw=%lld must be >= K and a multiple of 8", (long long)ldw);
+  if (N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: dimension too large");
+  if (N == 0 || K == 0) return FP8FG_OK;
+  if (!w || !q || !s) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: null pointer");
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s)) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128: pointers must be 16-byte aligned");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err = fp8fg::launch_quant_w_blocks(w, N, K, ldw, q, s, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_w_128x128 launch");
+  return FP8FG_OK;
+}
+
+int fp8_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,
+                         void* c, int c_dtype, int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: negative size");
+  if (sb_kind != FP8FG_SB_BLOCK_128x128 && sb_kind != FP8FG_SB_ROW_1x128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: unknown sb_kind %d", sb_kind);
+  if (c_dtype != FP8FG_OUT_F32 && c_dtype != FP8FG_OUT_BF16) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: unknown c_dtype %d", c_dtype);
+  if (K % 128 || N % 128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: K=%lld and N=%lld must be multiples of 128", (long long)K, (long long)N);
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: dimension too large");
+  if (M == 0 || N == 0) return FP8FG_OK;
+  if (!c) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: null output pointer");
+  if (!aligned16(c)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: pointers must be 16-byte aligned");
+  const size_t esize = c_dtype == FP8FG_OUT_BF16 ? 2 : 4;
+  if (K == 0) {
+    DeviceInfo dev;
+    if (int rc = current_device(&dev)) return rc;
+    cudaError_t err = cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * esize, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? FP8FG_OK : cuda_fail(err, "cudaMemsetAsync");
+  }
+  if (!qa || !sa || !qb || !sb) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: null pointer");
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: pointers must be 16-byte aligned");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype == FP8FG_OUT_BF16, M, N, K,
+                                                         reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
+  if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
+  return FP8FG_OK;
+}
+
+int fp8_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                     const int32_t* group_offsets, int E, int64_t Mtot, void* c, int c_dtype, int64_t N, int64_t K,
+                     fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (E < 1 || E > 1024) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: E=%d must be in 1..1024", E);
+  if (Mtot < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: negative size");
+  if (c_dtype != FP8FG_OUT_F32 && c_dtype != FP8FG_OUT_BF16) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: unknown c_dtype %d", c_dtype);
+  if (Mtot % 128 || N % 128 || K % 128) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: Mtot=%lld, N=%lld and K=%lld must be multiples of 128", (long long)Mtot, (long long)N, (long long)K);
+  if (Mtot > kMaxDim || N * E > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: dimension too large");
+  if (Mtot == 0 || N == 0) return FP8FG_OK;
+  if (K == 0) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: K must be positive");
+  if (!qa || !sa || !qb || !sb || !group_offsets || !c) return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: null pointer");
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb) || !aligned16(c) ||
+      (reinterpret_cast<uintptr_t>(group_offsets) & 3u))
+    return fail(FP8FG_ERR_ARG, "fp8_grouped_gemm: misaligned pointer");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  fp8fg::LaunchResult r = fp8fg::launch_grouped_gemm(qa, sa, qb, sb, group_offsets, E, Mtot, c,
+                                                     c_dtype == FP8FG_OUT_BF16, N, K,
+                                                     reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
+  if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
+  return FP8FG_OK;
+}
+
+int fp8fg_sync_status(fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  cudaError_t err = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
+  unsigned st = 0;
+  err = fp8fg::read_and_clear_status(&st);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the device status word");
+  if (st & 1u) return fail(FP8FG_ERR_TIMEOUT, "a device-side wait ran out of time (status 0x%x)", st);
+  if (st & 2u) return fail(FP8FG_ERR_DEVICE_ARG, "invalid group offsets on the device (status 0x%x)", st);
+  return FP8FG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// Launchers shared between the kernel files and the C ABI layer. Arguments have been
+// validated by the caller (abi.cu) before any of these is called.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8fg {
+
+cudaError_t launch_quant_act_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                                  cudaStream_t stream, int sm_count);
+cudaError_t launch_quant_act_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                                  cudaStream_t stream);
+cudaError_t launch_quant_w_blocks(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
+                                  cudaStream_t stream);
+
+// Status of a GEMM launch: cudaSuccess, or the failing CUDA call's error; `what`
+// names the failing step.
+struct LaunchResult {
+  cudaError_t err;
+  const char* what;
+};
+
+LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                                     int sb_kind, void* c, int c_bf16, int64_t M, int64_t N, int64_t K,
+                                     cudaStream_t stream, int sm_count);
+
+LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                                 const int32_t* offsets, int E, int64_t Mtot, void* c, int c_bf16, int64_t N,
+                                 int64_t K, cudaStream_t stream, int sm_count);
+
+}  // namespace fp8fg

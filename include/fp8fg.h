@@ -1,0 +1,148 @@
+/*
+ * fp8fg — fine-grained FP8 (E4M3) quantization and block-scaled FP8 GEMM on B300 (sm_103a).
+ *
+ * C ABI of the shared library libfp8fg.so. Every entry point takes plain device
+ * pointers and sizes; no PyTorch or C++ type crosses this boundary.
+ *
+ * What the operations are (knowledge-base pages on DeepSeek-V3 FP8 training):
+ *  - "Online quantization vs delayed quantization in DeepSeek-V3", item 1, and
+ *    "Unified E4M3 format in DeepSeek-V3", section on the fine-grained quantization
+ *    strategy: a scaling factor is computed on the fly for every 1x128 activation
+ *    tile and every 128x128 weight block, and all tensors use E4M3.
+ *  - "Advantages of using FP8 for GEMM operations in DeepSeek-V3", item 5: the FP8
+ *    GEMM promotes the tensor-core partial sums to FP32 at fixed intervals; item 8:
+ *    dense and MoE (grouped) FP8 GEMMs.
+ *
+ * Numerical definition (identical for every quantizer; a "group" is one 1x128 tile
+ * or one 128x128 block):
+ *    amax = max |x| over the group (exact)
+ *    s    = amax / 448          IEEE binary32 division, round to nearest even
+ *    q    = E4M3FN( x / s )     binary32 division, then round to nearest even into
+ *                               E4M3FN, saturating to +-448; the sign is kept, so a
+ *                               negative value that rounds to zero gives 0x80
+ *    a group with amax == 0 gets s = +0.0f and codes 0x00.
+ * E4M3FN is the OCP 8-bit float "E4M3" (bias 7, max 448, no infinities, NaN 0x7F/0xFF);
+ * codes are passed as uint8_t. Inputs are bfloat16 given as raw 16-bit words; NaN or
+ * infinite inputs give unspecified codes.
+ *
+ * Conventions shared by all entry points:
+ *  - Pointers are CUDA device pointers owned by the caller. The library never
+ *    allocates or frees memory. Outputs are overwritten, never accumulated into.
+ *  - Every data pointer must be 16-byte aligned; leading dimensions are in elements.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and do not
+ *    synchronize. They return FP8FG_OK (0) on success or a negative error code; on
+ *    error nothing has been launched and fp8fg_last_error() describes the problem.
+ *  - The GEMM kernels bound every device-side wait. A wait that runs out (about one
+ *    second) makes the kernel record FP8FG_ERR_TIMEOUT in a device status word and
+ *    return; fp8fg_sync_status() reports it. Invalid group offsets found on the
+ *    device are reported the same way (FP8FG_ERR_DEVICE_ARG).
+ *  - Empty problems (a zero dimension) return FP8FG_OK without launching.
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *fp8fg_stream_t;
+
+enum fp8fg_status {
+    FP8FG_OK = 0,
+    FP8FG_ERR_ARG = -1,        /* invalid argument detected on the host; nothing launched */
+    FP8FG_ERR_CUDA = -2,       /* a CUDA runtime or driver call failed */
+    FP8FG_ERR_TIMEOUT = -3,    /* a device-side wait ran out (from fp8fg_sync_status) */
+    FP8FG_ERR_DEVICE_ARG = -4, /* invalid device-resident argument (from fp8fg_sync_status) */
+    FP8FG_ERR_UNSUPPORTED = -5 /* the current device is not an sm_103 (B300) GPU */
+};
+
+enum fp8fg_out_dtype { FP8FG_OUT_F32 = 0, FP8FG_OUT_BF16 = 1 };
+
+enum fp8fg_sb_kind {
+    FP8FG_SB_BLOCK_128x128 = 0, /* sb[N/128][K/128]: one scale per 128x128 block of B */
+    FP8FG_SB_ROW_1x128 = 1      /* sb[N][K/128]:     one scale per 1x128 tile of B   */
+};
+
+/*
+ * Activation quantization in 1x128 tiles ("Online quantization vs delayed
+ * quantization in DeepSeek-V3", item 1; "Unified E4M3 format in DeepSeek-V3",
+ * fine-grained quantization strategy).
+ *
+ * x: bf16 [M][K], row stride ldx >= K elements (ldx % 8 == 0).
+ * transposed == 0: tiles run along K (a row's 128 consecutive columns).
+ *     Requires K % 128 == 0. Outputs q[M][K] (row stride K) and s[M][K/128].
+ *     x[m][k] ~= dec(q[m][k]) * s[m][k/128].
+ * transposed == 1: tiles run along M (128 consecutive rows of one column, e.g. 128
+ *     tokens of one feature, the reduction dimension of a weight-gradient GEMM; the
+ *     E4M3 page says the backward pass uses E4M3 too). Requires M % 128 == 0 and
+ *     K % 8 == 0. The result is stored transposed so that M is contiguous: q[K][M]
+ *     (row stride M) and s[K][M/128]; x[m][k] ~= dec(q[k][m]) * s[k][m/128].
+ * Returns FP8FG_ERR_ARG for a null pointer, misalignment or a shape rule broken.
+ */
+int fp8_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int transposed,
+                        uint8_t *q, float *s, fp8fg_stream_t stream);
+
+/*
+ * Weight quantization in 128x128 blocks (same passages as above).
+ *
+ * w: bf16 [N][K], row stride ldw >= K (ldw % 8 == 0); N % 128 == 0, K % 128 == 0.
+ * Outputs q[N][K] (row stride K) and s[N/128][K/128];
+ * w[n][k] ~= dec(q[n][k]) * s[n/128][k/128].
+ */
+int fp8_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                        uint8_t *q, float *s, fp8fg_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM C = A . B^T ("Advantages of using FP8 for GEMM operations in
+ * DeepSeek-V3", items 1, 5 and 8).
+ *
+ * qa: E4M3 [M][K] (row stride K), sa: f32 [M][K/128] (1x128 tiles of A).
+ * qb: E4M3 [N][K] (row stride K), sb: f32 scales of B, layout by sb_kind
+ *     (FP8FG_SB_BLOCK_128x128: [N/128][K/128]; FP8FG_SB_ROW_1x128: [N][K/128]).
+ * c:  [M][N] row-major, c_dtype FP8FG_OUT_F32 or FP8FG_OUT_BF16 (round to nearest even).
+ * For every 128-deep K chunk kb the tensor cores form the chunk's partial sum P in
+ * FP32, and C_acc[m][n] += P[m][n] * (sa[m][kb] * sb(n, kb)) is added in FP32.
+ * Requires K % 128 == 0 and N % 128 == 0; any M >= 0. K == 0 writes zeros.
+ */
+int fp8_blockscaled_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, const float *sb,
+                         int sb_kind, void *c, int c_dtype, int64_t M, int64_t N, int64_t K,
+                         fp8fg_stream_t stream);
+
+/*
+ * Grouped (MoE expert) block-scaled FP8 GEMM ("Advantages of using FP8 for GEMM
+ * operations in DeepSeek-V3", item 8: the MoE variant).
+ *
+ * qa: E4M3 [Mtot][K], sa: f32 [Mtot][K/128]. The rows of expert e are
+ *     group_offsets[e] .. group_offsets[e+1]-1 (contiguous, padded by the caller).
+ * group_offsets: DEVICE int32 [E+1], non-decreasing multiples of 128,
+ *     group_offsets[0] == 0 and group_offsets[E] == Mtot. Checked on the device: a
+ *     violation writes nothing useful and is reported by fp8fg_sync_status().
+ * qb: E4M3 [E][N][K], sb: f32 [E][N/128][K/128] (128x128 blocks per expert).
+ * c:  [Mtot][N]; row m of expert e is A[m] . B_e^T with the same per-chunk promotion
+ *     as fp8_blockscaled_gemm. Requires Mtot % 128 == 0, N % 128 == 0, K % 128 == 0.
+ */
+int fp8_grouped_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, const float *sb,
+                     const int32_t *group_offsets, int E, int64_t Mtot, void *c, int c_dtype,
+                     int64_t N, int64_t K, fp8fg_stream_t stream);
+
+/* Message for the last nonzero return on the calling thread ("" if none). */
+const char *fp8fg_last_error(void);
+
+/*
+ * Synchronize `stream`, then read and clear the current device's status word.
+ * Returns FP8FG_OK, FP8FG_ERR_TIMEOUT, FP8FG_ERR_DEVICE_ARG, or FP8FG_ERR_CUDA when
+ * the stream reports a CUDA error.
+ */
+int fp8fg_sync_status(fp8fg_stream_t stream);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int fp8fg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H */
