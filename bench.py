@@ -1,0 +1,471 @@
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
+
+Step (the timed unit): the dense-projection workload — X bf16 [4096, 7168] quantized in
+1x128 tiles, W bf16 [18432, 7168] quantized in 128x128 blocks, then the block-scaled
+FP8 GEMM C [4096, 18432] = X . W^T with BF16 output: three library calls through the C
+ABI, inputs resident in HBM. `value` is the step's GEMM FLOPs over the step time
+(TFLOP/s). The inputs (322 MB) exceed the 126 MB L2, so no flush is needed between
+steps. `e2e` repeats the step through the same calls with the inputs in pinned host
+memory: host-to-device copies of X and W and the device-to-host copy of C are inside
+the timed region. `rows` times every other kernel of the path alone (quantize-only
+1x128 [16384, 7168], transposed quantization and the weight-gradient GEMM, and the
+grouped MoE GEMM), each against its roofline; L2 is flushed between those runs.
+
+Under torchrun (N > 1) every rank runs the same step on its own GPU with its own data
+(weak scaling, no collective on the data path); the time is the max over ranks and
+`value` counts the work of all ranks.
+
+--impl reference times the CPU oracle on a bounded sample of the same workload on the
+host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% FP8 peak); 1x128 quantize GB/s (% HBM)"
+WORKLOAD = "dense projection: X bf16 [4096,7168] 1x128 + W bf16 [18432,7168] 128x128 quantize, block-scaled GEMM C[4096,18432] BF16"
+M, N, K = 4096, 18432, 7168
+GEMM_FLOPS = 2.0 * M * N * K
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate of the part (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "quant.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "fp8_fine_grained_cast_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/dram_traffic.json),
+    or None when absent or taken on other kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fp8fg_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+
+def dist_setup():
+    """(rank, world, local_rank) from the torchrun environment; a process group (NCCL
+    on GPUs, gloo otherwise) only when world > 1."""
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of a per-rank scalar (the elapsed time) over all ranks."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, world: int, max_elapsed_s: float) -> float:
+    """Whole-job throughput: the units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / max_elapsed_s
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from fp8_fine_grained_cast_b300 import inputs, ops
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+    fp8_peak = FP8_OVER_BF16 * peaks["bf16_tflops"]
+    fp8_peak_sus = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+    hbm_peak = peaks["hbm_gbs"]
+
+    d = inputs.dense(dev)
+    x, w = d.x, d.w
+    qx = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+    qw = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ops.quant_act_1x128(x, q=qx, s=sx)
+        if ev is not None:
+            ev[1].record(stream)
+        ops.quant_w_128x128(w, q=qw, s=sw)
+        if ev is not None:
+            ev[2].record(stream)
+        ops.blockscaled_gemm(qx, sx, qw, sw, ops.SB_BLOCK_128x128, torch.bfloat16, c=c)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    ops.sync_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ops.sync_status()
+    elapsed_ms = start.elapsed_time(stop)
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    ms_per_step = elapsed_ms / args.steps
+    value = aggregate_throughput(GEMM_FLOPS, world, ms_per_step / 1e3) / 1e12
+    t_qx = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_qw = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_gemm = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    gemm_tflops = GEMM_FLOPS / (t_gemm / 1e3) / 1e12
+    qx_bytes = M * K * 2 + M * K + M * (K // 128) * 4
+    qw_bytes = N * K * 2 + N * K + (N // 128) * (K // 128) * 4
+    clk = clocks.summary()
+
+    # ------------------------------------------------------------------ end to end
+    xh = x.cpu().pin_memory()
+    wh = w.cpu().pin_memory()
+    ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    xd, wd = torch.empty_like(x), torch.empty_like(w)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        ops.quant_act_1x128(xd, q=qx, s=sx)
+        ops.quant_w_128x128(wd, q=qw, s=sw)
+        ops.blockscaled_gemm(qx, sx, qw, sw, ops.SB_BLOCK_128x128, torch.bfloat16, c=c)
+        ch.copy_(c, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), dev) / e2e_steps
+    e2e_value = aggregate_throughput(GEMM_FLOPS, world, e2e_ms / 1e3) / 1e12
+    ops.sync_status()
+
+    rows = {} if args.no_rows else bench_rows(dev, stream, hbm_peak, fp8_peak, args)
+    launches = 3 * args.steps
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 (bf16 in, bf16 out)",
+        "data": "synthetic (seeded N(0,1) activations with 0.1% x100 outliers and zero tiles; N(0,0.02) weights)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "l2": "inputs 322 MB > 126 MB L2, no flush",
+                   "parallelism": f"replicas x{world} (weak, no data-path collective)"},
+        "frac_of_fp8_peak": round(value / fp8_peak, 4),
+        "roofline": {"bound": "tensor", "kernel": "blockscaled_gemm_kernel<256,4,0,bf16>",
+                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm_tflops / fp8_peak, 4),
+                     "peak_source": f"{peak_kind}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s (nominal FP8/BF16 ratio)",
+                     "frac_of_sustained": round(gemm_tflops / fp8_peak_sus, 4),
+                     "traffic": profiled_traffic("blockscaled_gemm_dense"),
+                     "algorithmic_flops_per_launch": GEMM_FLOPS, "avg_launch_ms": round(t_gemm, 4)},
+        "step_kernels_ms": {"quant_act_1x128": round(t_qx, 4), "quant_w_128x128": round(t_qw, 4),
+                            "blockscaled_gemm": round(t_gemm, 4)},
+        "quantize": {"act_1x128_GBps": round(qx_bytes / (t_qx / 1e3) / 1e9, 1),
+                     "act_frac_hbm": round(qx_bytes / (t_qx / 1e3) / 1e9 / hbm_peak, 4),
+                     "w_128x128_GBps": round(qw_bytes / (t_qw / 1e3) / 1e9, 1),
+                     "w_frac_hbm": round(qw_bytes / (t_qw / 1e3) / 1e9 / hbm_peak, 4),
+                     "hbm_peak_GBps": hbm_peak},
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": c.numel() * 2},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "rows": rows,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_sample_rows, args.cpu_sample_wrows)
+    return line
+
+
+def timed(fn, stream, iters, warm, flush):
+    """Mean device time (ms) of fn over `iters` runs, L2 flushed before each run."""
+    import torch
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
+def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
+    """Each remaining kernel of the path alone, against its roofline."""
+    import torch
+    from fp8_fine_grained_cast_b300 import inputs, ops
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    iters, warm = max(5, min(args.steps, 20)), 3
+    out = {}
+
+    xq = inputs.quant_only(dev)
+    nb = xq.numel() * 3 + xq.numel() // 128 * 4
+    t = timed(lambda: ops.quant_act_1x128(xq), stream, iters, warm, flush)
+    out["quant_act_1x128 [16384,7168]"] = {"bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1),
+                                          "frac": round(nb / t / 1e6 / hbm_peak, 4), "algorithmic_bytes": nb}
+    del xq
+
+    wg = inputs.wgrad(dev)
+    for name, tsr in (("dY [4096,2048]", wg.dy), ("X [4096,7168]", wg.x)):
+        nb = tsr.numel() * 3 + tsr.numel() // 128 * 4
+        t = timed(lambda: ops.quant_act_1x128(tsr, transposed=True), stream, iters, warm, flush)
+        out[f"quant_act_1x128 transposed {name}"] = {"bound": "hbm", "ms": round(t, 4),
+                                                     "GBps": round(nb / t / 1e6, 1),
+                                                     "frac": round(nb / t / 1e6 / hbm_peak, 4),
+                                                     "algorithmic_bytes": nb}
+    qdy, sdy = ops.quant_act_1x128(wg.dy, transposed=True)
+    qxt, sxt = ops.quant_act_1x128(wg.x, transposed=True)
+    fl = 2.0 * 2048 * 7168 * 4096
+    t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qxt, sxt, ops.SB_ROW_1x128, torch.float32), stream, iters, warm,
+              flush)
+    out["blockscaled_gemm wgrad 2048x7168x4096 f32"] = {"bound": "tensor", "ms": round(t, 4),
+                                                        "TFLOPs": round(fl / t / 1e9, 1),
+                                                        "frac": round(fl / t / 1e9 / fp8_peak, 4)}
+    del wg, qdy, sdy, qxt, sxt
+
+    m = inputs.moe(dev)
+    E, Ni, Kh = m.w.shape
+    qa, sa = ops.quant_act_1x128(m.a)
+    wflat = m.w.view(E * Ni, Kh)
+    nb = wflat.numel() * 3 + wflat.numel() // 16384 * 4
+    t = timed(lambda: ops.quant_w_128x128(wflat), stream, max(3, iters // 4), 1, flush)
+    out["quant_w_128x128 moe [256x2048,7168]"] = {"bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1),
+                                                  "frac": round(nb / t / 1e6 / hbm_peak, 4), "algorithmic_bytes": nb}
+    qw, sw = ops.quant_w_128x128(wflat)
+    qw3, sw3 = qw.view(E, Ni, Kh), sw.view(E, Ni // 128, Kh // 128)
+    mtot = m.a.shape[0]
+    c = torch.empty((mtot, Ni), dtype=torch.bfloat16, device=dev)
+    t = timed(lambda: ops.grouped_gemm(qa, sa, qw3, sw3, m.offsets, torch.bfloat16, c=c), stream, iters, warm, flush)
+    nb = qw.numel() + sw.numel() * 4 + qa.numel() + sa.numel() * 4 + c.numel() * 2
+    real_fl = 2.0 * m.real_rows * Ni * Kh
+    pad_fl = 2.0 * mtot * Ni * Kh
+    out["grouped_gemm moe 256 experts N2048 K7168 bf16"] = {
+        "bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1), "frac": round(nb / t / 1e6 / hbm_peak, 4),
+        "algorithmic_bytes": nb, "TFLOPs_real_rows": round(real_fl / t / 1e9, 1),
+        "TFLOPs_padded_rows": round(pad_fl / t / 1e9, 1), "real_rows": m.real_rows, "padded_rows": mtot}
+    ops.sync_status()
+    return out
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+def oracle_sample_step(x_rows, w_rows):
+    """One oracle pass over a sample of the dense-projection step: 1x128 quantization
+    of x_rows rows of X, 128x128 quantization of w_rows rows of W, and the float64 GEMM
+    of those rows. Returns (seconds, GEMM FLOPs of the sample)."""
+    import numpy as np
+    import torch
+    from fp8_fine_grained_cast_b300 import inputs
+    from oracle import fp8_oracle as O
+
+    d = inputs.dense("cpu", M=x_rows, N=w_rows)
+    xh = d.x.float().numpy()
+    wh = d.w.float().numpy()
+    t0 = time.perf_counter()
+    qx, sx = O.quant_act_1x128(xh)
+    qw, sw = O.quant_w_128x128(wh)
+    c = O.blockscaled_gemm(qx, sx, qw, sw)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(c).all()
+    del torch
+    return dt, 2.0 * x_rows * w_rows * K
+
+
+def cpu_baseline(x_rows, w_rows):
+    dt, fl = oracle_sample_step(x_rows, w_rows)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _blas_threads(), "kind": "oracle",
+            "sample": (f"X[:{x_rows}] 1x128 + W[:{w_rows}] 128x128 quantization (numpy, one thread) and their "
+                       f"float64 GEMM (BLAS, {_blas_threads()} threads): {dt:.2f} s for {fl:.3e} FLOP")}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        oracle_sample_step(args.ref_rows, args.ref_wrows)
+    times = []
+    fl = 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample_step(args.ref_rows, args.ref_wrows)
+        times.append(dt)
+    sec = sum(times) / len(times)
+    value = fl / sec / 1e12
+    cores = _blas_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"per step X[:{args.ref_rows}] and W[:{args.ref_wrows}] of the workload"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-kernel rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-rows", type=int, default=1024)
+    ap.add_argument("--cpu-sample-wrows", type=int, default=4608)
+    ap.add_argument("--ref-rows", type=int, default=256)
+    ap.add_argument("--ref-wrows", type=int, default=2048)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
+    args.steps = max(1, args.steps)
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -7,14 +7,15 @@
 // C = A . B^T, A [M][K] E4M3 with scales sa[M][K/128]; B [N][K] E4M3 with scales per
 // 128x128 block (sb[N/128][K/128]) or per 1x128 tile (sb[N][K/128]).
 //
-// Kernel structure (one persistent CTA per SM, 10 warps):
+// Kernel structure (one persistent CTA per SM, three warpgroups = 12 warps):
 //   warp 0     TMA producer: per K chunk, the A tile (128 x 128 B) and the B tile
 //              (BN x 128 B), 128-byte swizzled, into a STAGES-deep ring.
 //   warp 1     TMEM owner and MMA issuer: per chunk, 4 x tcgen05.mma (K = 32 each) into
 //              one of two TMEM accumulators (BN columns each), the first with the
 //              accumulate flag cleared, so that each accumulator holds exactly one
 //              chunk's partial sum P[m][n] = sum_{k in chunk} qa[m][k] qb[n][k].
-//   warps 2-9  promotion and epilogue: two groups of four warps; group g owns columns
+//   warps 2-3  idle (they complete the first warpgroup, which gives its registers up)
+//   warps 4-11 promotion and epilogue: two warpgroups; warpgroup g owns columns
 //              [g BN/2, (g+1) BN/2) of the tile and warp (w % 4) owns TMEM lanes (rows)
 //              32 (w % 4) .. +31. Per chunk: tcgen05.ld the partial sums, release the
 //              accumulator to the MMA warp, then C_acc += P * (sa[m][kb] * sb(n, kb)) in
@@ -68,9 +69,18 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kPromoWarps = 8;
+constexpr int kFirstPromoWarp = 4;
 constexpr int kStagingPerWarp = 4096;
+// Register split: the block is launched with kLaunchRegs per thread (384 x 168 =
+// 64512); warpgroup 0 (TMA, MMA) drops to 56 and the two promotion warpgroups rise to
+// 224, which sums to the same 4 x 32 x 56 + 8 x 32 x 224 = 64512. Per SM sub-partition
+// that is 56 + 224 + 224 registers for its three warps' lanes, within its 16K file.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsPromo = 224;
+static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
 struct GemmCfg {
@@ -99,7 +109,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
@@ -180,7 +190,9 @@ __global__ void __maxnreg__(200)
     }
   };
 
-  if (warp == 0) {
+  if (warp < kFirstPromoWarp) {
+   regs_decrease<kRegsControl>();
+   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && run) {
       tma_prefetch_map(&tmA);
@@ -246,10 +258,13 @@ __global__ void __maxnreg__(200)
       mbar_wait_drain(drain, 0);
     }
     __syncwarp();
-  } else if (run) {
+   }
+  } else {
+   regs_increase<kRegsPromo>();
+   if (run) {
     // ------------------------------------------------------------ promotion + epilogue
     constexpr int kHalf = Cfg::kHalf;
-    const int pw = warp - 2;
+    const int pw = warp - kFirstPromoWarp;
     const int g = pw >> 2;
     const int qd = warp & 3;
     const int row = 32 * qd + lane;
@@ -358,6 +373,7 @@ __global__ void __maxnreg__(200)
     }
     if (lane == 0) bulk_wait_group0();
     __syncwarp();
+   }
   }
 
   tc_fence_before();
@@ -410,6 +426,12 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   const size_t smem = Cfg::smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return {err, "cudaFuncSetAttribute(max dynamic shared memory)"};
+  // The in-kernel register split assumes the block starts with kLaunchRegs per thread;
+  // with fewer, the promotion warpgroups could never obtain their registers.
+  cudaFuncAttributes fa;
+  err = cudaFuncGetAttributes(&fa, kernel);
+  if (err != cudaSuccess) return {err, "cudaFuncGetAttributes"};
+  if (fa.numRegs != kLaunchRegs) return {cudaErrorInvalidConfiguration, "register count of the GEMM kernel"};
 
   CUtensorMap tmA, tmB, tmC;
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, K, kBK, kBM))
