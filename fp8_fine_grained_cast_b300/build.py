@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8fg.so")
-SOURCES = ["abi.cu", "quant.cu", "gemm.cu"]
+SOURCES = ["abi.cu", "quant.cu", "gemm.cu", "tensor_map.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 PUBLIC_HEADER = os.path.join(ROOT, "include", "fp8fg.h")
 

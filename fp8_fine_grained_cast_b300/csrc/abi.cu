@@ -8,10 +8,6 @@
 #include "../../include/fp8fg.h"
 #include "internal.h"
 
-namespace fp8fg {
-cudaError_t read_and_clear_status(unsigned* out);
-}
-
 namespace {
 
 thread_local char g_last_error[512] = "";
@@ -92,7 +88,8 @@ int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, in
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
   cudaError_t err = transposed
-                        ? fp8fg::launch_quant_act_cols(x, M, K, ldx, q, s, reinterpret_cast<cudaStream_t>(stream))
+                        ? fp8fg::launch_quant_act_cols(x, M, K, ldx, q, s, reinterpret_cast<cudaStream_t>(stream),
+                                                       dev.sm_count)
                         : fp8fg::launch_quant_act_rows(x, M, K, ldx, q, s, reinterpret_cast<cudaStream_t>(stream),
                                                        dev.sm_count);
   if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_act_1x128 launch");
@@ -172,9 +169,11 @@ int fp8fg_sync_status(fp8fg_stream_t stream) {
   g_last_error[0] = '\0';
   cudaError_t err = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "cudaStreamSynchronize");
-  unsigned st = 0;
-  err = fp8fg::read_and_clear_status(&st);
-  if (err != cudaSuccess) return cuda_fail(err, "reading the device status word");
+  unsigned st = 0, st_q = 0;
+  err = fp8fg::read_and_clear_gemm_status(&st);
+  if (err == cudaSuccess) err = fp8fg::read_and_clear_quant_status(&st_q);
+  if (err != cudaSuccess) return cuda_fail(err, "reading the device status words");
+  st |= st_q;
   if (st & 1u) return fail(FP8FG_ERR_TIMEOUT, "a device-side wait ran out of time (status 0x%x)", st);
   if (st & 2u) return fail(FP8FG_ERR_DEVICE_ARG, "invalid group offsets on the device (status 0x%x)", st);
   return FP8FG_OK;

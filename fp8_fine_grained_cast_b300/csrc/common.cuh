@@ -48,6 +48,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Arrive on `bar` only once `dep` has been computed. A release that hands a buffer back
+// to its producer must come after the buffer's loads have returned, not merely after
+// they were issued; passing a value computed from every loaded word makes the arrive
+// wait for them.
+__device__ __forceinline__ void mbar_arrive_after(uint64_t* bar, uint32_t dep) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)), "r"(dep) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -62,6 +70,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Device-side waits give up after this long.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Bits of a kernel file's device status word (read and cleared by fp8fg_sync_status).
+constexpr unsigned kStatusTimeout = 1u;      // a bounded wait ran out
+constexpr unsigned kStatusBadOffsets = 2u;   // grouped GEMM: invalid group offsets
+
+// Waits for the phase of `bar` with parity `parity`. Returns false if the CTA-wide
+// abort flag is raised or the time limit runs out; in the latter case it raises the
+// flag and records kStatusTimeout in *status, so that no wait can spin forever.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
 
 // Bounded wait used while shutting down after an abort: no flag check.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {

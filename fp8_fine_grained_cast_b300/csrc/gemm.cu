@@ -14,7 +14,9 @@
 //              one of two TMEM accumulators (BN columns each), the first with the
 //              accumulate flag cleared, so that each accumulator holds exactly one
 //              chunk's partial sum P[m][n] = sum_{k in chunk} qa[m][k] qb[n][k].
-//   warps 2-3  idle (they complete the first warpgroup, which gives its registers up)
+//   warp 2     scale loader: per chunk, the 128 row scales of A and the column (or
+//              column-block) scales of B into a shared-memory ring
+//   warp 3     idle (it completes the first warpgroup, which gives its registers up)
 //   warps 4-11 promotion and epilogue: two warpgroups; warpgroup g owns columns
 //              [g BN/2, (g+1) BN/2) of the tile and warp (w % 4) owns TMEM lanes (rows)
 //              32 (w % 4) .. +31. Per chunk: tcgen05.ld the partial sums, release the
@@ -27,42 +29,19 @@
 // CTA-wide abort flag and records a timeout in the device status word, every role
 // leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace fp8fg {
 
-// One status word per device; read and cleared by fp8fg_sync_status.
-__device__ unsigned int g_status = 0;
+// Status word of the GEMM kernels, one per device; read and cleared by fp8fg_sync_status.
+__device__ unsigned int g_gemm_status = 0;
 
-enum : unsigned {
-  kStatusTimeout = 1u,
-  kStatusBadOffsets = 2u,
-};
+__device__ __forceinline__ void record_status(unsigned bits) { atomicOr(&g_gemm_status, bits); }
 
-__device__ __forceinline__ void record_status(unsigned bits) { atomicOr(&g_status, bits); }
-
-// Bounded wait for the phase of `bar` with parity `parity`. Returns false if the
-// CTA's abort flag is raised or the time limit runs out (then it raises the flag and
-// records a timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        record_status(kStatusTimeout);
-        return false;
-      }
-    }
-  }
+  return mbar_wait(bar, parity, abort_flag, &g_gemm_status);
 }
 
 namespace {
@@ -85,22 +64,26 @@ static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsPromo <= kThreads * kLaunchR
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
 struct GemmCfg {
   static_assert(BN == 128 || BN == 256, "tile width");
-  static constexpr int kHalf = BN / 2;
-  static constexpr uint32_t kTmemCols = 2 * BN;
+  static constexpr int kHalf = BN / 2;               // columns per promotion warpgroup
+  static constexpr uint32_t kTmemCols = 2 * BN;      // two chunk accumulators
   static constexpr int kStageA = kBM * kBK;
   static constexpr int kStageB = BN * kBK;
+  // scale ring: per chunk, sa for the tile's 128 rows and sb for its columns (1x128
+  // scales of B) or its 128-column blocks (128x128 scales of B)
+  static constexpr int kSlots = (SB_KIND == 0 && STAGES >= 4) ? 4 : 8;
+  static constexpr int kSbPerSlot = SB_KIND == 1 ? BN : 4;
+  static constexpr int kSlotFloats = kBM + kSbPerSlot;
   static constexpr int kOffB = STAGES * kStageA;
   static constexpr int kOffStaging = kOffB + STAGES * kStageB;
-  static constexpr int kOffSb = kOffStaging + kPromoWarps * kStagingPerWarp;
-  static constexpr int kSbBytes = SB_KIND == 1 ? kPromoWarps * kHalf * 4 : 0;
-  static constexpr int kOffBar = kOffSb + kSbBytes;
-  // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kOffRing = kOffStaging + kPromoWarps * kStagingPerWarp;
+  static constexpr int kOffBar = kOffRing + kSlots * kSlotFloats * 4;
+  // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], scale_full[kSlots],
+  // scale_empty[kSlots], drain
+  static constexpr int kNumBars = 2 * STAGES + 4 + 2 * kSlots + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffsets = kOffMisc + 16;
-  static size_t smem_bytes(int E) { return 1024 + kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
-  // output box: 128 bytes of one row x 32 rows
-  static constexpr int kBoxCols = OUT_BF16 ? 64 : 32;
+  static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
+  static constexpr int kBoxCols = OUT_BF16 ? 64 : 32;  // output box: 128 bytes x 32 rows
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -115,14 +98,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
                             int K, int num_m_tiles, int num_n_tiles) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kSlots = Cfg::kSlots;
+  // The dynamic shared window starts 1024-byte aligned (checked below); the swizzled
+  // TMA tiles and the UMMA descriptors rely on it.
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint64_t* sfull = bars + 2 * STAGES + 4;
+  uint64_t* sempty = sfull + kSlots;
+  uint64_t* drain = sempty + kSlots;
+  float* ring = reinterpret_cast<float*>(smem + Cfg::kOffRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* bad_args = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
@@ -142,9 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kPromoWarps);
     }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&sfull[i], 32);
+      mbar_init(&sempty[i], kPromoWarps * 32);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
-    *bad_args = 0;
+    *bad_args = (smem_u32(smem) & 1023u) != 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -171,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const bool run = !*bad_args;
 
-  // tile t -> (m block, n block, expert)
+  // tile t -> (m block, n block, expert). Dense: m fastest, so that the CTAs working at
+  // the same time share B tiles (and A, which fits in L2). Grouped: n fastest, so that
+  // consecutive tiles share an expert's rows and concurrent tiles share its weights.
   auto tile_coords = [&](int t, int& m_blk, int& n_blk, int& e) {
     if constexpr (GROUPED) {
       n_blk = t % num_n_tiles;
@@ -191,189 +185,218 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp < kFirstPromoWarp) {
-   regs_decrease<kRegsControl>();
-   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && run) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB);
+    regs_decrease<kRegsControl>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- TMA producer
+      if (lane == 0 && run) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+          int m_blk, n_blk, e;
+          tile_coords(t, m_blk, n_blk, e);
+          const int a_row = m_blk * kBM;
+          const int b_row = (GROUPED ? e * N : 0) + n_blk * BN;
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t st = it % STAGES;
+            if (!mbar_wait(&empty[st], ((it / STAGES) & 1u) ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[st], Cfg::kStageA + Cfg::kStageB);
+            tma_load_2d(smem + st * Cfg::kStageA, &tmA, &full[st], kb * kBK, a_row);
+            tma_load_2d(smem + Cfg::kOffB + st * Cfg::kStageB, &tmB, &full[st], kb * kBK, b_row);
+            ++it;
+          }
+        }
+        if (!ok) {  // let the loads still in flight land before the CTA can exit
+          for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
+            mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0 && run) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t st = it % STAGES;
+            const uint32_t buf = it & 1u;
+            if (!mbar_wait(&full[st], (it / STAGES) & 1u, abort_flag) ||
+                !mbar_wait(&tempty[buf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + buf * BN;
+            const uint64_t a0 = sdesc_kmajor_sw128(smem_u32(smem + st * Cfg::kStageA));
+            const uint64_t b0 = sdesc_kmajor_sw128(smem_u32(smem + Cfg::kOffB + st * Cfg::kStageB));
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k) {
+              // advance 32 bytes (= 32 E4M3 values) along K inside the swizzle atom
+              mma_f8f6f4(d, a0 + 2u * k, b0 + 2u * k, idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[st]);
+            mma_commit(&tfull[buf]);
+            ++it;
+          }
+        }
+        mma_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+      __syncwarp();
+    } else if (warp == 2 && run) {
+      // ---------------------------------------------------------- scale loader
+      // Per chunk: sa[m0 .. m0+127][kb] and the B scales of the tile's columns into a
+      // ring slot, ahead of the promotion warps, so that no global load sits on their
+      // critical path.
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int m_blk, n_blk, e;
         tile_coords(t, m_blk, n_blk, e);
-        const int a_row = m_blk * kBM;
-        const int b_row = (GROUPED ? e * N : 0) + n_blk * BN;
+        const int m0 = m_blk * kBM;
+        const int n0 = n_blk * BN;
+        const int64_t step32 = static_cast<int64_t>(32) * KB;   // 32 rows of a scale matrix
+        const float* sa_col = sa + static_cast<int64_t>(m0 + lane) * KB;
+        const float* sb_col = SB_KIND == 1 ? sb + static_cast<int64_t>(n0 + lane) * KB
+                                           : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + n0 / kBM + lane) * KB;
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t st = it % STAGES;
-          const uint32_t use = it / STAGES;
-          if (!mbar_wait(&empty[st], (use & 1u) ^ 1u, abort_flag)) {
+          const uint32_t slot = it % kSlots;
+          if (!mbar_wait(&sempty[slot], ((it / kSlots) & 1u) ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[st], Cfg::kStageA + Cfg::kStageB);
-          tma_load_2d(smem + st * Cfg::kStageA, &tmA, &full[st], kb * kBK, a_row);
-          tma_load_2d(smem + Cfg::kOffB + st * Cfg::kStageB, &tmB, &full[st], kb * kBK, b_row);
+          float* sa_s = ring + slot * Cfg::kSlotFloats;
+          float* sb_s = sa_s + kBM;
+#pragma unroll
+          for (int i = 0; i < kBM / 32; ++i) {
+            sa_s[lane + 32 * i] = (m0 + lane + 32 * i < M) ? __ldg(sa_col + i * step32 + kb) : 0.0f;
+          }
+          if constexpr (SB_KIND == 0) {
+            if (lane < BN / kBM) sb_s[lane] = (n0 / kBM + lane < N / kBM) ? __ldg(sb_col + kb) : 0.0f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < BN / 32; ++i) {
+              sb_s[lane + 32 * i] = (n0 + lane + 32 * i < N) ? __ldg(sb_col + i * step32 + kb) : 0.0f;
+            }
+          }
+          mbar_arrive(&sfull[slot]);  // each lane publishes its own writes
           ++it;
         }
       }
-      if (!ok) {  // let the loads still in flight land before the CTA can exit
-        for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j) {
-          mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
-        }
-      }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && run) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+  } else {
+    regs_increase<kRegsPromo>();
+    if (run) {
+      // ---------------------------------------------------------- promotion + epilogue
+      constexpr int kHalf = Cfg::kHalf;
+      const int pw = warp - kFirstPromoWarp;
+      const int g = pw >> 2;
+      const int qd = warp & 3;
+      const int row = 32 * qd + lane;
+      uint8_t* stg = smem + Cfg::kOffStaging + pw * kStagingPerWarp;
+      const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int m_blk, n_blk, e;
+        tile_coords(t, m_blk, n_blk, e);
+        const int m0 = m_blk * kBM;
+        const int col0 = n_blk * BN + g * kHalf;
+
+        float acc[kHalf];
+#pragma unroll
+        for (int i = 0; i < kHalf; ++i) acc[i] = 0.0f;
+
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t st = it % STAGES;
-          const uint32_t use = it / STAGES;
+          const uint32_t slot = it % kSlots;
           const uint32_t buf = it & 1u;
-          const uint32_t buse = it >> 1;
-          if (!mbar_wait(&full[st], use & 1u, abort_flag) ||
-              !mbar_wait(&tempty[buf], (buse & 1u) ^ 1u, abort_flag)) {
+          if (!mbar_wait(&sfull[slot], (it / kSlots) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const float* sa_s = ring + slot * Cfg::kSlotFloats;
+          const float* sb_s = sa_s + kBM + g * kHalf;
+          const float sa_v = sa_s[row];
+          float sc = 0.0f;
+          if constexpr (SB_KIND == 0) sc = sa_v * sa_s[kBM + (g * kHalf) / kBM];
+          if (!mbar_wait(&tfull[buf], (it >> 1) & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + buf * BN;
-          const uint64_t a0 = sdesc_kmajor_sw128(smem_u32(smem + st * Cfg::kStageA));
-          const uint64_t b0 = sdesc_kmajor_sw128(smem_u32(smem + Cfg::kOffB + st * Cfg::kStageB));
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k) {
-            // advance 32 bytes (= 32 E4M3 values) along K inside the swizzle atom
-            mma_f8f6f4(d, a0 + 2u * k, b0 + 2u * k, idesc, k > 0 ? 1u : 0u);
-          }
-          mma_commit(&empty[st]);
-          mma_commit(&tfull[buf]);
-          ++it;
-        }
-      }
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0);
-    }
-    __syncwarp();
-   }
-  } else {
-   regs_increase<kRegsPromo>();
-   if (run) {
-    // ------------------------------------------------------------ promotion + epilogue
-    constexpr int kHalf = Cfg::kHalf;
-    const int pw = warp - kFirstPromoWarp;
-    const int g = pw >> 2;
-    const int qd = warp & 3;
-    const int row = 32 * qd + lane;
-    uint8_t* stg = smem + Cfg::kOffStaging + pw * kStagingPerWarp;
-    float* sbs = reinterpret_cast<float*>(smem + Cfg::kOffSb) + pw * kHalf;
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
-    uint32_t it = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-      int m_blk, n_blk, e;
-      tile_coords(t, m_blk, n_blk, e);
-      const int m0 = m_blk * kBM;
-      const int col0 = n_blk * BN + g * kHalf;
-      const int64_t grow = static_cast<int64_t>(m0) + row;
-      const bool row_ok = grow < M;
-      const float* sa_row = sa + grow * KB;
-      const float* sb_blk = sb;
-      bool sb_ok = col0 < N;
-      if constexpr (SB_KIND == 0) {
-        sb_blk = sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + col0 / kBM) * KB;
-      }
-
-      float acc[kHalf];
+          for (int h = 0; h < kHalf / 64; ++h) {
+            uint32_t v[64];
+            tmem_ld_32x32b_x32(t_lane + buf * BN + g * kHalf + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+            tmem_ld_32x32b_x32(t_lane + buf * BN + g * kHalf + 64 * h + 32,
+                               *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+            tmem_wait_ld();
+            if (h == kHalf / 64 - 1) {  // this warp has read the whole chunk accumulator
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[buf]);
+            }
+            float* a = acc + 64 * h;
+            if constexpr (SB_KIND == 0) {
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) acc[i] = 0.0f;
-
-      for (int kb = 0; kb < KB; ++kb) {
-        const float sa_v = row_ok ? __ldg(sa_row + kb) : 0.0f;
-        float sb_v = 0.0f;
-        if constexpr (SB_KIND == 0) {
-          sb_v = sb_ok ? __ldg(sb_blk + kb) : 0.0f;
-        } else {
-          __syncwarp();
+              for (int j = 0; j < 64; ++j) a[j] = fmaf(__uint_as_float(v[j]), sc, a[j]);
+            } else {
 #pragma unroll
-          for (int i = 0; i < kHalf / 32; ++i) {
-            const int n = col0 + 32 * i + lane;
-            sbs[32 * i + lane] = n < N ? __ldg(sb + static_cast<int64_t>(n) * KB + kb) : 0.0f;
-          }
-          __syncwarp();
-        }
-        const uint32_t buf = it & 1u;
-        const uint32_t buse = it >> 1;
-        if (!mbar_wait(&tfull[buf], buse & 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float sc = sa_v * sb_v;
-#pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(t_lane + buf * BN + g * kHalf + 32 * c, v);
-          tmem_wait_ld();
-          if (c == kHalf / 32 - 1) {  // all of this warp's reads of the accumulator are done
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
-          }
-          if constexpr (SB_KIND == 0) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(__uint_as_float(v[j]), sc, acc[32 * c + j]);
-          } else {
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 s4 = reinterpret_cast<const float4*>(sbs + 32 * c)[j4];
-              acc[32 * c + 4 * j4 + 0] = fmaf(__uint_as_float(v[4 * j4 + 0]), sa_v * s4.x, acc[32 * c + 4 * j4 + 0]);
-              acc[32 * c + 4 * j4 + 1] = fmaf(__uint_as_float(v[4 * j4 + 1]), sa_v * s4.y, acc[32 * c + 4 * j4 + 1]);
-              acc[32 * c + 4 * j4 + 2] = fmaf(__uint_as_float(v[4 * j4 + 2]), sa_v * s4.z, acc[32 * c + 4 * j4 + 2]);
-              acc[32 * c + 4 * j4 + 3] = fmaf(__uint_as_float(v[4 * j4 + 3]), sa_v * s4.w, acc[32 * c + 4 * j4 + 3]);
+              for (int j = 0; j < 64; j += 4) {
+                const float4 s4 = *reinterpret_cast<const float4*>(sb_s + 64 * h + j);
+                a[j + 0] = fmaf(__uint_as_float(v[j + 0]), sa_v * s4.x, a[j + 0]);
+                a[j + 1] = fmaf(__uint_as_float(v[j + 1]), sa_v * s4.y, a[j + 1]);
+                a[j + 2] = fmaf(__uint_as_float(v[j + 2]), sa_v * s4.z, a[j + 2]);
+                a[j + 3] = fmaf(__uint_as_float(v[j + 3]), sa_v * s4.w, a[j + 3]);
+              }
             }
           }
+          // each thread releases the scale slot once the values it read from it have
+          // been used (its last accumulator depends on them)
+          mbar_arrive_after(&sempty[slot], __float_as_uint(acc[kHalf - 1]));
+          ++it;
         }
-        ++it;
-      }
-      if (!ok) break;
+        if (!ok) break;
 
-      // -------------------------------------------------------- epilogue
-      constexpr int kBoxCols = Cfg::kBoxCols;
+        // ------------------------------------------------------ epilogue
+        constexpr int kBoxCols = Cfg::kBoxCols;
 #pragma unroll
-      for (int h = 0; h < kHalf / kBoxCols; ++h) {
-        if (col0 + h * kBoxCols >= N) break;
-        if (lane == 0) bulk_wait_group_read0();  // staging buffer free again
-        __syncwarp();
+        for (int h = 0; h < kHalf / kBoxCols; ++h) {
+          if (col0 + h * kBoxCols >= N) break;
+          if (lane == 0) bulk_wait_group_read0();  // staging buffer free again
+          __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 w;
-          if constexpr (OUT_BF16) {
-            const float* a = acc + h * 64 + 8 * c;
-            w = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                           pack_bf16x2(a[6], a[7]));
-          } else {
-            const float* a = acc + h * 32 + 4 * c;
-            w = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                           __float_as_uint(a[3]));
+          for (int c = 0; c < 8; ++c) {
+            uint4 w;
+            if constexpr (OUT_BF16) {
+              const float* a = acc + h * 64 + 8 * c;
+              w = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                             pack_bf16x2(a[6], a[7]));
+            } else {
+              const float* a = acc + h * 32 + 4 * c;
+              w = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                             __float_as_uint(a[3]));
+            }
+            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
           }
-          // 128-byte swizzle: 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
-          *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmC, stg, col0 + h * kBoxCols, m0 + 32 * qd);
-          bulk_commit_group();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stg, col0 + h * kBoxCols, m0 + 32 * qd);
+            bulk_commit_group();
+          }
         }
       }
+      if (lane == 0) bulk_wait_group0();
+      __syncwarp();
     }
-    if (lane == 0) bulk_wait_group0();
-    __syncwarp();
-   }
   }
 
   tc_fence_before();
@@ -385,37 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess) {
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-  });
-  return fn;
-}
-
-// 2D row-major tensor [rows][cols] with the given row pitch, box = box_cols x box_rows,
-// 128-byte swizzle, out-of-range elements read as zero.
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t cols, uint64_t rows,
-               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
 LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
@@ -434,13 +426,13 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   if (fa.numRegs != kLaunchRegs) return {cudaErrorInvalidConfiguration, "register count of the GEMM kernel"};
 
   CUtensorMap tmA, tmB, tmC;
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, K, kBK, kBM))
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, K, kBK, kBM, true))
     return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(A)"};
-  if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qb, K, b_rows, K, kBK, BN))
+  if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qb, K, b_rows, K, kBK, BN, true))
     return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(B)"};
   const uint64_t esize = OUT_BF16 ? 2 : 4;
   if (!encode_2d(&tmC, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M,
-                 N * esize, Cfg::kBoxCols, 32))
+                 N * esize, Cfg::kBoxCols, 32, true))
     return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(C)"};
 
   const int num_m = static_cast<int>((M + kBM - 1) / kBM);
@@ -475,13 +467,12 @@ LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8
   return run_gemm<256, 3, 0, false, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, stream, sm_count);
 }
 
-// Host access to the status word for fp8fg_sync_status.
-cudaError_t read_and_clear_status(unsigned* out) {
-  cudaError_t err = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned));
+cudaError_t read_and_clear_gemm_status(unsigned* out) {
+  cudaError_t err = cudaMemcpyFromSymbol(out, g_gemm_status, sizeof(unsigned));
   if (err != cudaSuccess) return err;
   if (*out) {
     const unsigned zero = 0;
-    err = cudaMemcpyToSymbol(g_status, &zero, sizeof(unsigned));
+    err = cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(unsigned));
   }
   return err;
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fp8fg {
@@ -10,7 +11,16 @@ namespace fp8fg {
 cudaError_t launch_quant_act_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
                                   cudaStream_t stream, int sm_count);
 cudaError_t launch_quant_act_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int sm_count);
+// 2D row-major tensor [rows][cols] with the given row pitch in bytes; box = box_cols x
+// box_rows elements; optional 128-byte swizzle; out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t cols, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+
+// Status words of the kernel files (timeouts, invalid device-side arguments).
+cudaError_t read_and_clear_gemm_status(unsigned* out);
+cudaError_t read_and_clear_quant_status(unsigned* out);
+
 cudaError_t launch_quant_w_blocks(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
                                   cudaStream_t stream);
 

@@ -1,8 +1,9 @@
 /* Exhaustive CPU check of the quantizers' fast quotient (test code, not the oracle).
  *
- * The kernels compute fl32(x / s) for s = fl32(amax / 448) as
- *     r = RN(1 / s); q0 = RN(x * r); e = fma(-q0, s, x); y = copysign(fma(e, r, q0), x)
- * whenever 2^-80 <= s <= 2^100 (Markstein's correction step), then round y to E4M3.
+ * The kernels compute -fl32(x / s) for s = fl32(amax / 448) as
+ *     nr = -RN(1 / s); q0n = RN(x * nr); e = fma(q0n, s, x); yn = fma(e, nr, q0n)
+ * whenever 2^-80 <= s <= 2^100 (Markstein's correction step on negated operands),
+ * round yn to E4M3 and flip the code's sign bit, i.e. they use y = -yn.
  * This program restates that formula with C99 binary32 arithmetic (fmaf rounds once)
  * and compares it with the IEEE quotient x / s over every pair of bf16 values with
  * 0 < amax and |x| <= amax whose scale lies in that range, both signs of x:
@@ -31,13 +32,13 @@ int main(int argc, char **argv) {
         const float amax = from_bits((uint32_t)ab << 16);
         const float s = amax / 448.0f;
         if (!(s >= 0x1p-80f && s <= 0x1p+100f)) continue;
-        const float r = 1.0f / s;
+        const float nr = -(1.0f / s);
         for (uint32_t xb = 0; xb <= (uint32_t)ab; ++xb) {
             for (int sign = 0; sign < 2; ++sign) {
                 const float x = from_bits((xb << 16) | (sign ? 0x80000000u : 0u));
-                const float q0 = x * r;
-                const float e = fmaf(-q0, s, x);
-                const float y = copysignf(fmaf(e, r, q0), x);
+                const float q0n = x * nr;
+                const float e = fmaf(q0n, s, x);
+                const float y = -fmaf(e, nr, q0n);
                 const float want = x / s;
                 ++checked;
                 int ok;
