@@ -53,12 +53,13 @@ constexpr int kPromoWarps = 8;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kStagingPerWarp = 4096;
 // Register split: the block is launched with kLaunchRegs per thread (384 x 168 =
-// 64512); warpgroup 0 (TMA, MMA) drops to 56 and the two promotion warpgroups rise to
-// 224, which sums to the same 4 x 32 x 56 + 8 x 32 x 224 = 64512. Per SM sub-partition
-// that is 56 + 224 + 224 registers for its three warps' lanes, within its 16K file.
+// 64512); warpgroup 0 (TMA, MMA, scale loader) drops to 40 and the two promotion
+// warpgroups rise to 232, which sums to the same 4 x 32 x 40 + 8 x 32 x 232 = 64512. Per
+// SM sub-partition that is 40 + 232 + 232 registers for its three warps' lanes, within
+// its 16K register file.
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kRegsControl = 56;
-constexpr uint32_t kRegsPromo = 224;
+constexpr uint32_t kRegsControl = 40;
+constexpr uint32_t kRegsPromo = 232;
 static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
@@ -132,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sfull[i], 32);
-      mbar_init(&sempty[i], kPromoWarps * 32);
+      mbar_init(&sempty[i], SB_KIND == 0 ? kPromoWarps : kPromoWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -309,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = m_blk * kBM;
         const int col0 = n_blk * BN + g * kHalf;
 
-        float acc[kHalf];
+        // FP32 accumulators of this thread's row, in pairs for the packed FMAs
+        float2 acc2[kHalf / 2];
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < kHalf / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+        float* acc = reinterpret_cast<float*>(acc2);
 
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t slot = it % kSlots;
@@ -324,42 +327,78 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* sb_s = sa_s + kBM + g * kHalf;
           const float sa_v = sa_s[row];
           float sc = 0.0f;
-          if constexpr (SB_KIND == 0) sc = sa_v * sa_s[kBM + (g * kHalf) / kBM];
+          if constexpr (SB_KIND == 0) {
+            sc = sa_v * sa_s[kBM + (g * kHalf) / kBM];
+            // Both scales of this chunk are now in registers: release the slot. The
+            // warp-wide reduction makes lane 0's arrive wait until every lane's scale
+            // product (hence its two shared-memory reads) has completed.
+            const uint32_t dep = __reduce_or_sync(0xFFFFFFFFu, __float_as_uint(sc));
+            if (lane == 0) mbar_arrive_after(&sempty[slot], dep);
+          }
           if (!mbar_wait(&tfull[buf], (it >> 1) & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t t_col = t_lane + buf * BN + g * kHalf;
+          if constexpr (SB_KIND == 0) {
+            // rounds of 64 columns: two x32 loads, one wait, 32 packed FMAs with the
+            // chunk's scale product sa[m][kb] * sb[n block][kb]
+            const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-          for (int h = 0; h < kHalf / 64; ++h) {
-            uint32_t v[64];
-            tmem_ld_32x32b_x32(t_lane + buf * BN + g * kHalf + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-            tmem_ld_32x32b_x32(t_lane + buf * BN + g * kHalf + 64 * h + 32,
-                               *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-            tmem_wait_ld();
-            if (h == kHalf / 64 - 1) {  // this warp has read the whole chunk accumulator
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&tempty[buf]);
+            for (int p = 0; p < kHalf / 64; ++p) {
+              uint32_t w0[32], w1[32];
+              tmem_ld_32x32b_x32(t_col + 64 * p, w0);
+              tmem_ld_32x32b_x32(t_col + 64 * p + 32, w1);
+              tmem_wait_ld_tied(w0);
+              tmem_wait_ld_tied(w1);
+              if (p == kHalf / 64 - 1) {  // this warp has read the whole chunk accumulator
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+              }
+              float2* a = acc2 + 32 * p;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                a[j] = __ffma2_rn(make_float2(__uint_as_float(w0[2 * j]), __uint_as_float(w0[2 * j + 1])), sc2, a[j]);
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                a[16 + j] =
+                    __ffma2_rn(make_float2(__uint_as_float(w1[2 * j]), __uint_as_float(w1[2 * j + 1])), sc2, a[16 + j]);
+              }
             }
-            float* a = acc + 64 * h;
-            if constexpr (SB_KIND == 0) {
+          } else {
+            // rounds of 32 columns: one x32 load, one wait, per-column scale products
+            // sa[m][kb] * sb[n][kb] and 16 packed FMAs
+            const float2 sa2 = make_float2(sa_v, sa_v);
 #pragma unroll
-              for (int j = 0; j < 64; ++j) a[j] = fmaf(__uint_as_float(v[j]), sc, a[j]);
-            } else {
+            for (int p = 0; p < kHalf / 32; ++p) {
+              uint32_t w[32];
+              tmem_ld_32x32b_x32(t_col + 32 * p, w);
+              tmem_wait_ld_tied(w);
+              if (p == kHalf / 32 - 1) {  // this warp has read the whole chunk accumulator
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+              }
+              float2* a = acc2 + 16 * p;
 #pragma unroll
-              for (int j = 0; j < 64; j += 4) {
-                const float4 s4 = *reinterpret_cast<const float4*>(sb_s + 64 * h + j);
-                a[j + 0] = fmaf(__uint_as_float(v[j + 0]), sa_v * s4.x, a[j + 0]);
-                a[j + 1] = fmaf(__uint_as_float(v[j + 1]), sa_v * s4.y, a[j + 1]);
-                a[j + 2] = fmaf(__uint_as_float(v[j + 2]), sa_v * s4.z, a[j + 2]);
-                a[j + 3] = fmaf(__uint_as_float(v[j + 3]), sa_v * s4.w, a[j + 3]);
+              for (int j = 0; j < 16; j += 2) {
+                const float4 s4 = *reinterpret_cast<const float4*>(sb_s + 32 * p + 2 * j);
+                const float2 t0 = __fmul2_rn(make_float2(s4.x, s4.y), sa2);
+                const float2 t1 = __fmul2_rn(make_float2(s4.z, s4.w), sa2);
+                a[j] = __ffma2_rn(make_float2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), t0, a[j]);
+                a[j + 1] =
+                    __ffma2_rn(make_float2(__uint_as_float(w[2 * j + 2]), __uint_as_float(w[2 * j + 3])), t1, a[j + 1]);
               }
             }
           }
-          // each thread releases the scale slot once the values it read from it have
-          // been used (its last accumulator depends on them)
-          mbar_arrive_after(&sempty[slot], __float_as_uint(acc[kHalf - 1]));
+          if constexpr (SB_KIND == 1) {
+            // each thread releases the scale slot once the values it read from it have
+            // been used (its last accumulator depends on them)
+            mbar_arrive_after(&sempty[slot], __float_as_uint(acc[kHalf - 1]));
+          }
           ++it;
         }
         if (!ok) break;
