@@ -44,6 +44,7 @@ SIGNATURES = {
     "fp8fg_last_error": (ctypes.c_char_p, []),
     "fp8fg_sync_status": (_I, [_P]),
     "fp8fg_version": (_I, []),
+    "fp8fg_selftest_wait_timeout": (_I, [_P]),
 }
 
 
@@ -100,6 +101,10 @@ def fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):
 
 def fp8_grouped_gemm(qa, sa, qb, sb, group_offsets, E, Mtot, c, c_dtype, N, K, stream):
     return _check(lib().fp8_grouped_gemm(qa, sa, qb, sb, group_offsets, E, Mtot, c, c_dtype, N, K, stream))
+
+
+def fp8fg_selftest_wait_timeout(stream):
+    return _check(lib().fp8fg_selftest_wait_timeout(stream))
 
 
 def fp8fg_sync_status(stream):

@@ -165,6 +165,15 @@ int fp8_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, cons
   return FP8FG_OK;
 }
 
+int fp8fg_selftest_wait_timeout(fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err = fp8fg::launch_wait_timeout_selftest(reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "fp8fg_selftest_wait_timeout launch");
+  return FP8FG_OK;
+}
+
 int fp8fg_sync_status(fp8fg_stream_t stream) {
   g_last_error[0] = '\0';
   cudaError_t err = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -506,6 +506,29 @@ LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8
   return run_gemm<256, 3, 0, false, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, stream, sm_count);
 }
 
+namespace {
+
+// One thread waits on a barrier that never completes; the bounded wait gives up after
+// kWaitLimitNs and records kStatusTimeout in the GEMM status word.
+__global__ void wait_timeout_selftest_kernel() {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_flag);
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_gemm_status(unsigned* out) {
   cudaError_t err = cudaMemcpyFromSymbol(out, g_gemm_status, sizeof(unsigned));
   if (err != cudaSuccess) return err;

@@ -20,6 +20,7 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
 // Status words of the kernel files (timeouts, invalid device-side arguments).
 cudaError_t read_and_clear_gemm_status(unsigned* out);
 cudaError_t read_and_clear_quant_status(unsigned* out);
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
 
 cudaError_t launch_quant_w_blocks(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
                                   cudaStream_t stream);

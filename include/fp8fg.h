@@ -32,9 +32,10 @@
  *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and do not
  *    synchronize. They return FP8FG_OK (0) on success or a negative error code; on
  *    error nothing has been launched and fp8fg_last_error() describes the problem.
- *  - The GEMM kernels bound every device-side wait. A wait that runs out (about one
- *    second) makes the kernel record FP8FG_ERR_TIMEOUT in a device status word and
- *    return; fp8fg_sync_status() reports it. Invalid group offsets found on the
+ *  - The pipelined kernels (the GEMMs and the transposed quantizer) bound every
+ *    device-side wait. A wait that runs out (about one second) makes the kernel record
+ *    a timeout in a device status word and return; fp8fg_sync_status() reports it as
+ *    FP8FG_ERR_TIMEOUT. Invalid group offsets found on the
  *    device are reported the same way (FP8FG_ERR_DEVICE_ARG).
  *  - Empty problems (a zero dimension) return FP8FG_OK without launching.
  */
@@ -132,11 +133,22 @@ int fp8_grouped_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, cons
 const char *fp8fg_last_error(void);
 
 /*
- * Synchronize `stream`, then read and clear the current device's status word.
+ * Synchronize `stream`, then read and clear the current device's status words.
  * Returns FP8FG_OK, FP8FG_ERR_TIMEOUT, FP8FG_ERR_DEVICE_ARG, or FP8FG_ERR_CUDA when
  * the stream reports a CUDA error.
  */
 int fp8fg_sync_status(fp8fg_stream_t stream);
+
+/*
+ * Self-test of the device-side failure detection (no counterpart on the pages: it
+ * exercises this library's own safety mechanism). Launches one small kernel that waits,
+ * with the bounded wait every pipelined kernel here uses, on a shared-memory barrier
+ * nothing ever arrives at. After about one second the wait gives up and records a
+ * timeout in the device status word; the kernel then returns normally, so the context
+ * stays usable. A following fp8fg_sync_status(stream) returns FP8FG_ERR_TIMEOUT and
+ * clears the word. Returns FP8FG_OK when the launch succeeded.
+ */
+int fp8fg_selftest_wait_timeout(fp8fg_stream_t stream);
 
 /* Library version, e.g. 100 for 0.1.0. */
 int fp8fg_version(void);
