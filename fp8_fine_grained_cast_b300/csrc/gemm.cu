@@ -92,6 +92,92 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// G consecutive floats (16-, 8- or 4-byte aligned) or zeros.
+template <int G>
+struct Vec;
+template <>
+struct Vec<1> {
+  float v[1];
+  __device__ __forceinline__ void load(const float* p, bool ok) { v[0] = ok ? __ldg(p) : 0.0f; }
+};
+template <>
+struct Vec<2> {
+  float v[2];
+  __device__ __forceinline__ void load(const float* p, bool ok) {
+    const float2 t = ok ? __ldg(reinterpret_cast<const float2*>(p)) : make_float2(0.0f, 0.0f);
+    v[0] = t.x;
+    v[1] = t.y;
+  }
+};
+template <>
+struct Vec<4> {
+  float v[4];
+  __device__ __forceinline__ void load(const float* p, bool ok) {
+    const float4 t = ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    v[0] = t.x;
+    v[1] = t.y;
+    v[2] = t.z;
+    v[3] = t.w;
+  }
+};
+
+// Scale-loader loop of loader warp `li` (0 or 1): groups of G chunks, alternate groups
+// per warp; slot of chunk c is c % kSlots (kSlots >= 2 G). Requires KB % G == 0 so that
+// a group never straddles two tiles.
+template <int G, typename Cfg, bool GROUPED, int SB_KIND, typename Coords>
+__device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M, int N, int num_tiles,
+                                                 const Coords& tile_coords, const float* __restrict__ sa,
+                                                 const float* __restrict__ sb, float* ring, uint64_t* sfull,
+                                                 uint64_t* sempty, volatile int* abort_flag) {
+  constexpr int kSlots = Cfg::kSlots;
+  constexpr int BN = Cfg::kStageB / kBK;
+  uint32_t it = 0;
+  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    int m_blk, n_blk, e;
+    tile_coords(t, m_blk, n_blk, e);
+    const int m0 = m_blk * kBM;
+    const int n0 = n_blk * BN;
+    const int64_t step32 = static_cast<int64_t>(32) * KB;  // 32 rows of a scale matrix
+    const float* sa_col = sa + static_cast<int64_t>(m0 + lane) * KB;
+    const float* sb_col = SB_KIND == 1
+                              ? sb + static_cast<int64_t>(n0 + lane) * KB
+                              : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + n0 / kBM + lane) * KB;
+    for (int kb0 = 0; kb0 < KB; kb0 += G, it += G) {
+      if (static_cast<int>((it / G) & 1u) != li) continue;
+      for (int g = 0; g < G; ++g) {
+        const uint32_t c = it + g;
+        if (!mbar_wait(&sempty[c % kSlots], ((c / kSlots) & 1u) ^ 1u, abort_flag)) return;
+      }
+#pragma unroll
+      for (int i = 0; i < kBM / 32; ++i) {
+        const int r = lane + 32 * i;
+        Vec<G> x;
+        x.load(sa_col + i * step32 + kb0, m0 + r < M);
+#pragma unroll
+        for (int g = 0; g < G; ++g) ring[((it + g) % kSlots) * Cfg::kSlotFloats + r] = x.v[g];
+      }
+      if constexpr (SB_KIND == 0) {
+        if (lane < BN / kBM) {
+          Vec<G> x;
+          x.load(sb_col + kb0, n0 / kBM + lane < N / kBM);
+#pragma unroll
+          for (int g = 0; g < G; ++g) ring[((it + g) % kSlots) * Cfg::kSlotFloats + kBM + lane] = x.v[g];
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i) {
+          Vec<G> x;
+          x.load(sb_col + i * step32 + kb0, n0 + lane + 32 * i < N);
+#pragma unroll
+          for (int g = 0; g < G; ++g) ring[((it + g) % kSlots) * Cfg::kSlotFloats + kBM + lane + 32 * i] = x.v[g];
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) mbar_arrive(&sfull[(it + g) % kSlots]);  // each lane its own writes
+    }
+  }
+}
+
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -100,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             int K, int num_m_tiles, int num_n_tiles) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
+  constexpr int kGroup = kSlots / 2;   // chunks per scale-loader group (two groups in flight)
   // The dynamic shared window starts 1024-byte aligned (checked below); the swizzled
   // TMA tiles and the UMMA descriptors rely on it.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -250,45 +337,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(drain, 0);
       }
       __syncwarp();
-    } else if (warp == 2 && run) {
-      // ---------------------------------------------------------- scale loader
-      // Per chunk: sa[m0 .. m0+127][kb] and the B scales of the tile's columns into a
-      // ring slot, ahead of the promotion warps, so that no global load sits on their
-      // critical path.
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        int m_blk, n_blk, e;
-        tile_coords(t, m_blk, n_blk, e);
-        const int m0 = m_blk * kBM;
-        const int n0 = n_blk * BN;
-        const int64_t step32 = static_cast<int64_t>(32) * KB;   // 32 rows of a scale matrix
-        const float* sa_col = sa + static_cast<int64_t>(m0 + lane) * KB;
-        const float* sb_col = SB_KIND == 1 ? sb + static_cast<int64_t>(n0 + lane) * KB
-                                           : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + n0 / kBM + lane) * KB;
-        for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t slot = it % kSlots;
-          if (!mbar_wait(&sempty[slot], ((it / kSlots) & 1u) ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          float* sa_s = ring + slot * Cfg::kSlotFloats;
-          float* sb_s = sa_s + kBM;
-#pragma unroll
-          for (int i = 0; i < kBM / 32; ++i) {
-            sa_s[lane + 32 * i] = (m0 + lane + 32 * i < M) ? __ldg(sa_col + i * step32 + kb) : 0.0f;
-          }
-          if constexpr (SB_KIND == 0) {
-            if (lane < BN / kBM) sb_s[lane] = (n0 / kBM + lane < N / kBM) ? __ldg(sb_col + kb) : 0.0f;
-          } else {
-#pragma unroll
-            for (int i = 0; i < BN / 32; ++i) {
-              sb_s[lane + 32 * i] = (n0 + lane + 32 * i < N) ? __ldg(sb_col + i * step32 + kb) : 0.0f;
-            }
-          }
-          mbar_arrive(&sfull[slot]);  // each lane publishes its own writes
-          ++it;
-        }
+    } else if (run) {
+      // ---------------------------------------------------------- scale loaders
+      // Warps 2 and 3 fill the scale ring ahead of the promotion warps, so that no
+      // global load sits on their critical path: per chunk, sa[m0 .. m0+127][kb] and the
+      // B scales of the tile's columns (1x128) or column blocks (128x128). Chunks go in
+      // groups of kGroup, fetched with one vector load per scale row; the two warps take
+      // alternate groups, so two groups of loads are in flight while the promotion warps
+      // consume a third.
+      const int li = warp - 2;
+      if (KB % kGroup == 0) {
+        load_scales_impl<kGroup, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, sa, sb, ring,
+                                                        sfull, sempty, abort_flag);
+      } else {
+        load_scales_impl<1, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, sa, sb, ring, sfull,
+                                                   sempty, abort_flag);
       }
     }
   } else {
@@ -487,12 +550,31 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 
 }  // namespace
 
+// Tile width: 256 columns unless 128-column tiles finish in fewer tile-rounds of the
+// persistent grid (time ~ rounds x tile width), e.g. when 256-column tiles leave the
+// last wave nearly empty.
+static bool prefer_narrow_tiles(int64_t M, int64_t N, int sm_count) {
+  const int64_t mt = (M + kBM - 1) / kBM;
+  const int64_t r256 = (mt * ((N + 255) / 256) + sm_count - 1) / sm_count;
+  const int64_t r128 = (mt * ((N + 127) / 128) + sm_count - 1) / sm_count;
+  return r128 * 128 < r256 * 256;
+}
+
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                      int sb_kind, void* c, int c_bf16, int64_t M, int64_t N, int64_t K,
                                      cudaStream_t stream, int sm_count) {
+  const bool narrow = false && prefer_narrow_tiles(M, N, sm_count);
   if (sb_kind == 0) {
+    if (narrow) {
+      if (c_bf16) return run_gemm<128, 6, 0, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+      return run_gemm<128, 6, 0, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+    }
     if (c_bf16) return run_gemm<256, 4, 0, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
     return run_gemm<256, 4, 0, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+  }
+  if (narrow) {
+    if (c_bf16) return run_gemm<128, 5, 1, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+    return run_gemm<128, 5, 1, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
   }
   if (c_bf16) return run_gemm<256, 3, 1, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
   return run_gemm<256, 3, 1, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
