@@ -23,8 +23,9 @@
 //              accumulator to the MMA warp, then C_acc += P * (sa[m][kb] * sb(n, kb)) in
 //              FP32 registers. While they promote chunk kb the tensor cores already
 //              compute chunk kb+1 into the other accumulator. After the last chunk the
-//              accumulators are rounded to the output type, staged in shared memory with
-//              the 128-byte swizzle and written by TMA stores.
+//              accumulators are rounded to the output type, transposed through a small
+//              swizzled shared-memory buffer per warp and written with coalesced 16-byte
+//              stores (the TMA unit stays free for the operand loads).
 // Every mbarrier wait is bounded (about one second); a wait that runs out raises a
 // CTA-wide abort flag and records a timeout in the device status word, every role
 // leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
@@ -48,35 +49,46 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 128;
-constexpr int kThreads = 384;
-constexpr int kPromoWarps = 8;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kStagingPerWarp = 4096;
-// Register split: the block is launched with kLaunchRegs per thread (384 x 168 =
-// 64512); warpgroup 0 (TMA, MMA, scale loader) drops to 40 and the two promotion
-// warpgroups rise to 232, which sums to the same 4 x 32 x 40 + 8 x 32 x 232 = 64512. Per
-// SM sub-partition that is 40 + 232 + 232 registers for its three warps' lanes, within
-// its 16K register file.
-constexpr int kLaunchRegs = 168;
-constexpr uint32_t kRegsControl = 40;
-constexpr uint32_t kRegsPromo = 232;
-static_assert(4 * 32 * kRegsControl + 8 * 32 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
+
+// Layout by tile width BN. Warpgroup 0 holds the TMA producer, the MMA issuer and the two
+// scale loaders; two promotion warpgroups follow, each owning kCols = BN / 2 columns.
+// Register split: the block is launched with kLaunchRegs per thread (384 threads x 168 =
+// 64512); warpgroup 0 then drops to 40 and the promotion warpgroups rise to 232, which
+// sums to the same 4 x 32 x 40 + 8 x 32 x 232 = 64512. Per SM sub-partition the lanes of
+// its three warps get 40 + 232 + 232 = 504 registers, within its 16K register file.
+// (A three-warpgroup layout with 192-column tiles, one TMEM round trip per chunk and
+// warp, measured slower on the dense workload and is not built.)
+template <int BN>
+struct WarpLayout {
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static constexpr int kPWG = 2;
+  static constexpr int kCols = BN / kPWG;
+  static constexpr int kPromoWarps = 4 * kPWG;
+  static constexpr int kThreads = 128 * (1 + kPWG);
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr uint32_t kRegsControl = 40;
+  static constexpr uint32_t kRegsPromo = 232;
+  static_assert(4 * 32 * kRegsControl + kPromoWarps * 32 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
+  static constexpr uint32_t kTmemBuf = BN;  // column stride of the two chunk accumulators
+  static constexpr uint32_t kTmemCols = 2 * kTmemBuf;
+};
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
-struct GemmCfg {
-  static_assert(BN == 128 || BN == 256, "tile width");
-  static constexpr int kHalf = BN / 2;               // columns per promotion warpgroup
-  static constexpr uint32_t kTmemCols = 2 * BN;      // two chunk accumulators
+struct GemmCfg : WarpLayout<BN> {
+  using L = WarpLayout<BN>;
   static constexpr int kStageA = kBM * kBK;
   static constexpr int kStageB = BN * kBK;
-  // scale ring: per chunk, sa for the tile's 128 rows and sb for its columns (1x128
-  // scales of B) or its 128-column blocks (128x128 scales of B)
-  static constexpr int kSlots = (SB_KIND == 0 && STAGES >= 4) ? 4 : 8;
+  // scale ring: per chunk, sa for the tile's 128 rows and the B scales: one per column
+  // (1x128 scales of B) or one per promotion warpgroup (128x128 scales of B; a
+  // warpgroup's columns lie in a single 128-column block)
+  static constexpr int kSlots = (BN == 256 && SB_KIND == 0 && STAGES >= 4) ? 4 : 8;  // 4: shared memory is full
   static constexpr int kSbPerSlot = SB_KIND == 1 ? BN : 4;
   static constexpr int kSlotFloats = kBM + kSbPerSlot;
   static constexpr int kOffB = STAGES * kStageA;
   static constexpr int kOffStaging = kOffB + STAGES * kStageB;
-  static constexpr int kOffRing = kOffStaging + kPromoWarps * kStagingPerWarp;
+  static constexpr int kOffRing = kOffStaging + L::kPromoWarps * kStagingPerWarp;
   static constexpr int kOffBar = kOffRing + kSlots * kSlotFloats * 4;
   // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], scale_full[kSlots],
   // scale_empty[kSlots], drain
@@ -84,7 +96,8 @@ struct GemmCfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffsets = kOffMisc + 16;
   static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
-  static constexpr int kBoxCols = OUT_BF16 ? 64 : 32;  // output box: 128 bytes x 32 rows
+  static constexpr int kBoxCols = OUT_BF16 ? 64 : 32;  // epilogue box: 32 rows x 128 bytes
+  static_assert(L::kCols % kBoxCols == 0, "epilogue boxes");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -139,9 +152,9 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
     const int n0 = n_blk * BN;
     const int64_t step32 = static_cast<int64_t>(32) * KB;  // 32 rows of a scale matrix
     const float* sa_col = sa + static_cast<int64_t>(m0 + lane) * KB;
-    const float* sb_col = SB_KIND == 1
-                              ? sb + static_cast<int64_t>(n0 + lane) * KB
-                              : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + n0 / kBM + lane) * KB;
+    const float* sb_col =
+        SB_KIND == 1 ? sb + static_cast<int64_t>(n0 + lane) * KB
+                     : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + (n0 + lane * Cfg::kCols) / kBM) * KB;
     for (int kb0 = 0; kb0 < KB; kb0 += G, it += G) {
       if (static_cast<int>((it / G) & 1u) != li) continue;
       for (int g = 0; g < G; ++g) {
@@ -157,9 +170,9 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
         for (int g = 0; g < G; ++g) ring[((it + g) % kSlots) * Cfg::kSlotFloats + r] = x.v[g];
       }
       if constexpr (SB_KIND == 0) {
-        if (lane < BN / kBM) {
+        if (lane < Cfg::kPWG) {  // the 128x128 block of promotion warpgroup `lane`'s columns
           Vec<G> x;
-          x.load(sb_col + kb0, n0 / kBM + lane < N / kBM);
+          x.load(sb_col + kb0, (n0 + lane * Cfg::kCols) / kBM < N / kBM);
 #pragma unroll
           for (int g = 0; g < G; ++g) ring[((it + g) % kSlots) * Cfg::kSlotFloats + kBM + lane] = x.v[g];
         }
@@ -179,13 +192,14 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
 }
 
 template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmC, const float* __restrict__ sa,
+                            void* __restrict__ c_out, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
                             int K, int num_m_tiles, int num_n_tiles) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
+  constexpr int kPromoWarps = Cfg::kPromoWarps;
   constexpr int kGroup = kSlots / 2;   // chunks per scale-loader group (two groups in flight)
   // The dynamic shared window starts 1024-byte aligned (checked below); the swizzled
   // TMA tiles and the UMMA descriptors rely on it.
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp < kFirstPromoWarp) {
-    regs_decrease<kRegsControl>();
+    regs_decrease<Cfg::kRegsControl>();
     if (warp == 0) {
       // ---------------------------------------------------------- TMA producer
       if (lane == 0 && run) {
@@ -320,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + buf * BN;
+            const uint32_t d = tmem_base + buf * Cfg::kTmemBuf;
             const uint64_t a0 = sdesc_kmajor_sw128(smem_u32(smem + st * Cfg::kStageA));
             const uint64_t b0 = sdesc_kmajor_sw128(smem_u32(smem + Cfg::kOffB + st * Cfg::kStageB));
 #pragma unroll
@@ -355,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    regs_increase<kRegsPromo>();
+    regs_increase<Cfg::kRegsPromo>();
     if (run) {
       // ---------------------------------------------------------- promotion + epilogue
-      constexpr int kHalf = Cfg::kHalf;
+      constexpr int kCols = Cfg::kCols;
       const int pw = warp - kFirstPromoWarp;
       const int g = pw >> 2;
       const int qd = warp & 3;
@@ -371,12 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int m_blk, n_blk, e;
         tile_coords(t, m_blk, n_blk, e);
         const int m0 = m_blk * kBM;
-        const int col0 = n_blk * BN + g * kHalf;
+        const int col0 = n_blk * BN + g * kCols;
 
         // FP32 accumulators of this thread's row, in pairs for the packed FMAs
-        float2 acc2[kHalf / 2];
+        float2 acc2[kCols / 2];
 #pragma unroll
-        for (int i = 0; i < kHalf / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         float* acc = reinterpret_cast<float*>(acc2);
 
         for (int kb = 0; kb < KB; ++kb) {
@@ -387,11 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const float* sa_s = ring + slot * Cfg::kSlotFloats;
-          const float* sb_s = sa_s + kBM + g * kHalf;
+          const float* sb_s = sa_s + kBM + g * kCols;
           const float sa_v = sa_s[row];
           float sc = 0.0f;
           if constexpr (SB_KIND == 0) {
-            sc = sa_v * sa_s[kBM + (g * kHalf) / kBM];
+            sc = sa_v * sa_s[kBM + g];
             // Both scales of this chunk are now in registers: release the slot. The
             // warp-wide reduction makes lane 0's arrive wait until every lane's scale
             // product (hence its two shared-memory reads) has completed.
@@ -403,19 +417,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t t_col = t_lane + buf * BN + g * kHalf;
+          const uint32_t t_col = t_lane + buf * Cfg::kTmemBuf + g * kCols;
           if constexpr (SB_KIND == 0) {
             // rounds of 64 columns: two x32 loads, one wait, 32 packed FMAs with the
             // chunk's scale product sa[m][kb] * sb[n block][kb]
             const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-            for (int p = 0; p < kHalf / 64; ++p) {
+            for (int p = 0; p < kCols / 64; ++p) {
               uint32_t w0[32], w1[32];
               tmem_ld_32x32b_x32(t_col + 64 * p, w0);
               tmem_ld_32x32b_x32(t_col + 64 * p + 32, w1);
               tmem_wait_ld_tied(w0);
               tmem_wait_ld_tied(w1);
-              if (p == kHalf / 64 - 1) {  // this warp has read the whole chunk accumulator
+              if (p == kCols / 64 - 1) {  // this warp has read its whole chunk slice
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -436,11 +450,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // sa[m][kb] * sb[n][kb] and 16 packed FMAs
             const float2 sa2 = make_float2(sa_v, sa_v);
 #pragma unroll
-            for (int p = 0; p < kHalf / 32; ++p) {
+            for (int p = 0; p < kCols / 32; ++p) {
               uint32_t w[32];
               tmem_ld_32x32b_x32(t_col + 32 * p, w);
               tmem_wait_ld_tied(w);
-              if (p == kHalf / 32 - 1) {  // this warp has read the whole chunk accumulator
+              if (p == kCols / 32 - 1) {  // this warp has read its whole chunk slice
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -460,44 +474,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (SB_KIND == 1) {
             // each thread releases the scale slot once the values it read from it have
             // been used (its last accumulator depends on them)
-            mbar_arrive_after(&sempty[slot], __float_as_uint(acc[kHalf - 1]));
+            mbar_arrive_after(&sempty[slot], __float_as_uint(acc[kCols - 1]));
           }
           ++it;
         }
         if (!ok) break;
 
         // ------------------------------------------------------ epilogue
+        // Per box of 32 rows x 128 bytes: each lane writes its row into the warp's
+        // staging buffer (16-byte chunk c of row r at chunk position c ^ (r % 8), so
+        // that both the row-wise writes and the column-wise reads below hit all 32
+        // banks), then the warp reads it back four rows per instruction and stores
+        // four full 128-byte lines per instruction to C. The stores go through the
+        // load/store path, not the TMA unit, which is busy with the operand loads.
         constexpr int kBoxCols = Cfg::kBoxCols;
+        uint8_t* c_bytes = reinterpret_cast<uint8_t*>(c_out);
+        constexpr int kEsize = OUT_BF16 ? 2 : 4;
 #pragma unroll
-        for (int h = 0; h < kHalf / kBoxCols; ++h) {
-          if (col0 + h * kBoxCols >= N) break;
-          if (lane == 0) bulk_wait_group_read0();  // staging buffer free again
-          __syncwarp();
+        for (int h = 0; h < kCols / kBoxCols; ++h) {
+          const int box_col = col0 + h * kBoxCols;
+          if (box_col >= N) break;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int ch = 0; ch < 8; ++ch) {
             uint4 w;
             if constexpr (OUT_BF16) {
-              const float* a = acc + h * 64 + 8 * c;
+              const float* a = acc + h * 64 + 8 * ch;
               w = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                              pack_bf16x2(a[6], a[7]));
             } else {
-              const float* a = acc + h * 32 + 4 * c;
+              const float* a = acc + h * 32 + 4 * ch;
               w = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
                              __float_as_uint(a[3]));
             }
-            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk position c ^ (r % 8)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = w;
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((ch ^ (lane & 7)) << 4)) = w;
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmC, stg, col0 + h * kBoxCols, m0 + 32 * qd);
-            bulk_commit_group();
+          const int ch = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ((ch ^ (r & 7)) << 4));
+            const int64_t grow = static_cast<int64_t>(m0) + 32 * qd + r;
+            if (grow < M) {
+              *reinterpret_cast<uint4*>(c_bytes + (grow * N + box_col) * kEsize + ch * 16) = w;
+            }
           }
+          __syncwarp();
         }
       }
-      if (lane == 0) bulk_wait_group0();
-      __syncwarp();
     }
   }
 
@@ -525,23 +549,19 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   cudaFuncAttributes fa;
   err = cudaFuncGetAttributes(&fa, kernel);
   if (err != cudaSuccess) return {err, "cudaFuncGetAttributes"};
-  if (fa.numRegs != kLaunchRegs) return {cudaErrorInvalidConfiguration, "register count of the GEMM kernel"};
+  if (fa.numRegs != Cfg::kLaunchRegs) return {cudaErrorInvalidConfiguration, "register count of the GEMM kernel"};
 
-  CUtensorMap tmA, tmB, tmC;
+  CUtensorMap tmA, tmB;
   if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, qa, K, M, K, kBK, kBM, true))
     return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(A)"};
   if (!encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, qb, K, b_rows, K, kBK, BN, true))
     return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(B)"};
-  const uint64_t esize = OUT_BF16 ? 2 : 4;
-  if (!encode_2d(&tmC, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c, N, M,
-                 N * esize, Cfg::kBoxCols, 32, true))
-    return {cudaErrorInvalidValue, "cuTensorMapEncodeTiled(C)"};
 
   const int num_m = static_cast<int>((M + kBM - 1) / kBM);
   const int num_n = static_cast<int>((N + BN - 1) / BN);
   const int64_t tiles = static_cast<int64_t>(num_m) * num_n;
   const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
-  kernel<<<grid, kThreads, smem, stream>>>(tmA, tmB, tmC, sa, sb, offsets, E, static_cast<int>(M),
+  kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, sa, sb, offsets, E, static_cast<int>(M),
                                            static_cast<int>(N), static_cast<int>(K), num_m, num_n);
   err = cudaGetLastError();
   if (err != cudaSuccess) return {err, "kernel launch"};
@@ -550,31 +570,15 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 
 }  // namespace
 
-// Tile width: 256 columns unless 128-column tiles finish in fewer tile-rounds of the
-// persistent grid (time ~ rounds x tile width), e.g. when 256-column tiles leave the
-// last wave nearly empty.
-static bool prefer_narrow_tiles(int64_t M, int64_t N, int sm_count) {
-  const int64_t mt = (M + kBM - 1) / kBM;
-  const int64_t r256 = (mt * ((N + 255) / 256) + sm_count - 1) / sm_count;
-  const int64_t r128 = (mt * ((N + 127) / 128) + sm_count - 1) / sm_count;
-  return r128 * 128 < r256 * 256;
-}
-
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                      int sb_kind, void* c, int c_bf16, int64_t M, int64_t N, int64_t K,
                                      cudaStream_t stream, int sm_count) {
-  const bool narrow = false && prefer_narrow_tiles(M, N, sm_count);
+  // 128 x 256 tiles throughout: 128-column tiles, tried for the weight-gradient shape
+  // whose 256-column tiles leave a nearly empty last wave, measured slower (the fixed
+  // per-chunk cost of the promotion handshake is paid twice as often).
   if (sb_kind == 0) {
-    if (narrow) {
-      if (c_bf16) return run_gemm<128, 6, 0, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-      return run_gemm<128, 6, 0, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-    }
     if (c_bf16) return run_gemm<256, 4, 0, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
     return run_gemm<256, 4, 0, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-  }
-  if (narrow) {
-    if (c_bf16) return run_gemm<128, 5, 1, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-    return run_gemm<128, 5, 1, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
   }
   if (c_bf16) return run_gemm<256, 3, 1, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
   return run_gemm<256, 3, 1, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);

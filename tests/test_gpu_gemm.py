@@ -49,7 +49,8 @@ def run_gemm(qa, sa, qb, sb, sb_kind, out_dtype, device):
 
 @pytest.mark.parametrize("sb_kind", [O.SB_BLOCK_128x128, O.SB_ROW_1x128])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 384, 640), (1, 256, 256), (520, 1024, 1152)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 384, 640), (1, 256, 256), (520, 1024, 1152),
+                                   (200, 768, 384)])
 def test_gemm_matches_oracle(cuda_device, sb_kind, out_dtype, M, N, K):
     rng = np.random.default_rng(M * 7 + N * 3 + K)
     qa, sa, qb, sb = random_quantized(rng, M, N, K, sb_kind)
