@@ -61,16 +61,16 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(kernel: str):
-    """DRAM bytes per launch recorded from an ncu capture (profiles/dram_traffic.json),
+    """DRAM bytes per launch recorded from an ncu capture (profiles/dram_traffic.txt),
     or None when absent or taken on other kernel sources."""
-    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    ent = d.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
-        return None
-    return ent.get("bytes_per_launch")
+    for line in open(p):
+        parts = line.split()
+        if len(parts) == 3 and not line.startswith("#") and parts[0] == kernel:
+            return int(parts[2]) if parts[1] == kernel_source_hash() else None
+    return None
 
 
 class ClockSampler:
