@@ -354,6 +354,35 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                                         "frac": round(fl / t / 1e9 / fp8_peak, 4)}
     del wg, qdy, sdy, qxt, sxt
 
+    # both orientations of X from one read (fprop 1x128 along K + wgrad tiles along M)
+    xd = inputs.dense(dev, N=128).x                                          # [4096, 7168]
+    nb = xd.numel() * 4 + 2 * (xd.numel() // 128) * 4
+    t = timed(lambda: ops.quant_act_1x128_dual(xd), stream, iters, warm, flush)
+    t2 = timed(lambda: (ops.quant_act_1x128(xd), ops.quant_act_1x128(xd, transposed=True)), stream, iters, warm,
+               flush)
+    out["quant_act_1x128_dual X [4096,7168]"] = {"bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1),
+                                                 "frac": round(nb / t / 1e6 / hbm_peak, 4), "algorithmic_bytes": nb,
+                                                 "ms_two_single_calls": round(t2, 4)}
+    del xd
+
+    # dX = dY . W of the dense projection: W quantized once in both orientations
+    dg = inputs.dgrad(dev)                                                   # dY [4096,18432], W [18432,7168]
+    nb = dg.w.numel() * 4 + 2 * (dg.w.numel() // 16384) * 4
+    t = timed(lambda: ops.quant_w_128x128_dual(dg.w), stream, iters, warm, flush)
+    out["quant_w_128x128_dual W [18432,7168]"] = {"bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1),
+                                                  "frac": round(nb / t / 1e6 / hbm_peak, 4), "algorithmic_bytes": nb}
+    qdy, sdy = ops.quant_act_1x128(dg.dy)
+    _, _, qwt, swt = ops.quant_w_128x128_dual(dg.w)
+    del dg
+    dx = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+    fl = 2.0 * 4096 * 7168 * 18432
+    t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qwt, swt, ops.SB_BLOCK_128x128, torch.bfloat16, c=dx), stream,
+              iters, warm, flush)
+    out["blockscaled_gemm dgrad 4096x7168x18432 bf16"] = {"bound": "tensor", "ms": round(t, 4),
+                                                          "TFLOPs": round(fl / t / 1e9, 1),
+                                                          "frac": round(fl / t / 1e9 / fp8_peak, 4)}
+    del qdy, sdy, qwt, swt, dx
+
     m = inputs.moe(dev)
     E, Ni, Kh = m.w.shape
     qa, sa = ops.quant_act_1x128(m.a)
@@ -492,6 +521,22 @@ def run_case(args):
         del wg
         fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_ROW_1x128, torch.float32)
         work = {"flops": 2.0 * 2048 * 7168 * 4096}
+    elif case == "qdual":
+        x = inputs.dense(dev, N=128).x
+        fn = lambda: ops.quant_act_1x128_dual(x)
+        work = {"bytes": x.numel() * 4 + 2 * (x.numel() // 128) * 4}
+    elif case == "wdual":
+        w = inputs.dense(dev, M=128).w
+        fn = lambda: ops.quant_w_128x128_dual(w)
+        work = {"bytes": w.numel() * 4 + 2 * (w.numel() // 16384) * 4}
+    elif case == "dgrad":
+        dg = inputs.dgrad(dev)
+        a, sa = ops.quant_act_1x128(dg.dy)
+        _, _, b, sb = ops.quant_w_128x128_dual(dg.w)
+        del dg
+        c = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_BLOCK_128x128, torch.bfloat16, c=c)
+        work = {"flops": 2.0 * 4096 * 7168 * 18432}
     elif case == "grouped":
         m = inputs.moe(dev, tokens=1024, experts=64)
         E, Ni, Kh = m.w.shape
@@ -529,7 +574,7 @@ def main():
     ap.add_argument("--cpu-sample-wrows", type=int, default=4608)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--ref-wrows", type=int, default=2048)
-    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped"],
+    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad"],
                     help="time one kernel on its workload instead of the step (for profiling)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()

@@ -39,6 +39,8 @@ _I = ctypes.c_int
 SIGNATURES = {
     "fp8_quant_act_1x128": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P]),
     "fp8_quant_w_128x128": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
+    "fp8_quant_act_1x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "fp8_quant_w_128x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_blockscaled_gemm": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _P, _I, _I64, _I64, _P]),
     "fp8fg_last_error": (ctypes.c_char_p, []),
@@ -93,6 +95,14 @@ def fp8_quant_act_1x128(x, M, K, ldx, transposed, q, s, stream):
 
 def fp8_quant_w_128x128(w, N, K, ldw, q, s, stream):
     return _check(lib().fp8_quant_w_128x128(w, N, K, ldw, q, s, stream))
+
+
+def fp8_quant_act_1x128_dual(x, M, K, ldx, q, s, qt, st, stream):
+    return _check(lib().fp8_quant_act_1x128_dual(x, M, K, ldx, q, s, qt, st, stream))
+
+
+def fp8_quant_w_128x128_dual(w, N, K, ldw, q, s, qt, st, stream):
+    return _check(lib().fp8_quant_w_128x128_dual(w, N, K, ldw, q, s, qt, st, stream))
 
 
 def fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):

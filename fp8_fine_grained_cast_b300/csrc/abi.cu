@@ -113,6 +113,45 @@ int fp8_quant_w_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, ui
   return FP8FG_OK;
 }
 
+int fp8_quant_act_1x128_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                             uint8_t* qt, float* st, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (M < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: negative size");
+  if (M % 128 || K % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: M=%lld and K=%lld must be multiples of 128", (long long)M, (long long)K);
+  if (ldx < K || ldx % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: ldx=%lld must be >= K and a multiple of 8", (long long)ldx);
+  if (M > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: dimension too large");
+  if (M == 0 || K == 0) return FP8FG_OK;
+  if (!x || !q || !s || !qt || !st) return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: null pointer");
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s) || !aligned16(qt) || !aligned16(st)) {
+    return fail(FP8FG_ERR_ARG, "fp8_quant_act_1x128_dual: pointers must be 16-byte aligned");
+  }
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err = fp8fg::launch_quant_act_dual(x, M, K, ldx, q, s, qt, st, reinterpret_cast<cudaStream_t>(stream),
+                                                 dev.sm_count);
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_act_1x128_dual launch");
+  return FP8FG_OK;
+}
+
+int fp8_quant_w_128x128_dual(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
+                             uint8_t* qt, float* st, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: negative size");
+  if (N % 128 || K % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: N=%lld and K=%lld must be multiples of 128", (long long)N, (long long)K);
+  if (ldw < K || ldw % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: ldw=%lld must be >= K and a multiple of 8", (long long)ldw);
+  if (N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: dimension too large");
+  if (N == 0 || K == 0) return FP8FG_OK;
+  if (!w || !q || !s || !qt || !st) return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: null pointer");
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s) || !aligned16(qt) || !aligned16(st)) {
+    return fail(FP8FG_ERR_ARG, "fp8_quant_w_128x128_dual: pointers must be 16-byte aligned");
+  }
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err = fp8fg::launch_quant_w_dual(w, N, K, ldw, q, s, qt, st, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_w_128x128_dual launch");
+  return FP8FG_OK;
+}
+
 int fp8_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,
                          void* c, int c_dtype, int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream) {
   g_last_error[0] = '\0';

@@ -12,6 +12,10 @@ cudaError_t launch_quant_act_rows(const uint16_t* x, int64_t M, int64_t K, int64
                                   cudaStream_t stream, int sm_count);
 cudaError_t launch_quant_act_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
                                   cudaStream_t stream, int sm_count);
+// Both orientations from one read: q[M][K], s[M][K/128] (tiles along K) and
+// qt[K][M], st[K][M/128] (tiles along M); M and K multiples of 128.
+cudaError_t launch_quant_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
+                                  uint8_t* qt, float* st, cudaStream_t stream, int sm_count);
 // 2D row-major tensor [rows][cols] with the given row pitch in bytes; box = box_cols x
 // box_rows elements; optional 128-byte swizzle; out-of-range elements read as zero.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t cols, uint64_t rows,
@@ -24,6 +28,10 @@ cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
 
 cudaError_t launch_quant_w_blocks(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
                                   cudaStream_t stream);
+// Both orientations of the 128x128 block quantization: q[N][K], s[N/128][K/128] and
+// qt[K][N], st[K/128][N/128].
+cudaError_t launch_quant_w_dual(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
+                                uint8_t* qt, float* st, cudaStream_t stream);
 
 // Status of a GEMM launch: cudaSuccess, or the failing CUDA call's error; `what`
 // names the failing step.

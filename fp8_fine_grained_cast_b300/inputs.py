@@ -18,6 +18,8 @@ Workloads (one scale group = 1x128 activation tile or 128x128 weight block):
               are its tokens in token order, zero-padded to a multiple of 128 rows;
               W [256, 2048, 7168] ~ N(0, 0.02)                            (seed 3)
   wgrad       dY [4096, 2048] ~ N(0, 1e-3), X [4096, 7168] ~ N(0, 1)     (seed 4)
+  dgrad       backward of the dense projection: dY [4096, 18432] ~ N(0, 1e-3),
+              W [18432, 7168] ~ N(0, 0.02); dX = dY . W [4096, 7168]      (seed 5)
 """
 from __future__ import annotations
 
@@ -25,7 +27,7 @@ from dataclasses import dataclass
 
 import torch
 
-CONFIG_SEEDS = {"tiny": 0, "quant": 1, "dense": 2, "moe": 3, "wgrad": 4}
+CONFIG_SEEDS = {"tiny": 0, "quant": 1, "dense": 2, "moe": 3, "wgrad": 4, "dgrad": 5}
 
 
 def _gen(device, seed: int, tensor_id: int) -> torch.Generator:
@@ -157,6 +159,17 @@ def wgrad(device="cpu", T: int = 4096, dout: int = 2048, din: int = 7168) -> WGr
     return WGrad(dy=gaussian_bf16((T, dout), 1e-3, device, s, 0), x=gaussian_bf16((T, din), 1.0, device, s, 1))
 
 
+@dataclass
+class DGrad:
+    dy: torch.Tensor
+    w: torch.Tensor
+
+
+def dgrad(device="cpu", T: int = 4096, dout: int = 18432, din: int = 7168) -> DGrad:
+    s = CONFIG_SEEDS["dgrad"]
+    return DGrad(dy=gaussian_bf16((T, dout), 1e-3, device, s, 0), w=gaussian_bf16((dout, din), 0.02, device, s, 1))
+
+
 def gemm_flops(M: int, N: int, K: int) -> float:
     return 2.0 * M * N * K
 
@@ -165,5 +178,5 @@ def moe_real_flops(m: MoE, inter: int, hidden: int) -> float:
     return 2.0 * m.real_rows * inter * hidden
 
 
-__all__ = ["CONFIG_SEEDS", "tiny", "quant_only", "dense", "moe", "wgrad", "gaussian_bf16", "activation_bf16",
+__all__ = ["CONFIG_SEEDS", "tiny", "quant_only", "dense", "moe", "wgrad", "dgrad", "gaussian_bf16", "activation_bf16",
            "zipf_topk_routing", "gemm_flops", "moe_real_flops"]

@@ -66,6 +66,42 @@ def quant_w_128x128(w: torch.Tensor, q=None, s=None):
     return q, s
 
 
+def quant_act_1x128_dual(x: torch.Tensor, out=None):
+    """x bf16 [M, K] -> (q [M, K], s [M, K/128], qt [K, M], st [K, M/128]) from one read of x:
+    the results of quant_act_1x128(x) and quant_act_1x128(x, transposed=True)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _rows_contiguous(x, "x")
+    M, K = x.shape
+    if out is None:
+        dev = x.device
+        out = (torch.empty((M, K), dtype=torch.uint8, device=dev),
+               torch.empty((M, K // 128), dtype=torch.float32, device=dev),
+               torch.empty((K, M), dtype=torch.uint8, device=dev),
+               torch.empty((K, M // 128), dtype=torch.float32, device=dev))
+    q, s, qt, st = out
+    _lib.fp8_quant_act_1x128_dual(x.data_ptr(), M, K, x.stride(0), q.data_ptr(), s.data_ptr(), qt.data_ptr(),
+                                  st.data_ptr(), _stream())
+    return q, s, qt, st
+
+
+def quant_w_128x128_dual(w: torch.Tensor, out=None):
+    """w bf16 [N, K] -> (q [N, K], s [N/128, K/128], qt [K, N], st [K/128, N/128]): the 128x128
+    block quantization of w and its transpose (the B operand of dX = dY . W)."""
+    _need(w, torch.bfloat16, "w", 2)
+    _rows_contiguous(w, "w")
+    N, K = w.shape
+    if out is None:
+        dev = w.device
+        out = (torch.empty((N, K), dtype=torch.uint8, device=dev),
+               torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
+               torch.empty((K, N), dtype=torch.uint8, device=dev),
+               torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev))
+    q, s, qt, st = out
+    _lib.fp8_quant_w_128x128_dual(w.data_ptr(), N, K, w.stride(0), q.data_ptr(), s.data_ptr(), qt.data_ptr(),
+                                  st.data_ptr(), _stream())
+    return q, s, qt, st
+
+
 def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out_dtype=torch.bfloat16, c=None):
     """C = A . B^T from E4M3 codes and scales; C [M, N] in bf16 or float32."""
     for t, n, dt, nd in ((qa, "qa", torch.uint8, 2), (sa, "sa", torch.float32, 2), (qb, "qb", torch.uint8, 2),

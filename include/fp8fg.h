@@ -97,6 +97,35 @@ int fp8_quant_w_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
                         uint8_t *q, float *s, fp8fg_stream_t stream);
 
 /*
+ * Both orientations of the 1x128 activation quantization from one read of x (the
+ * transposed copy feeds the weight-gradient GEMM; "Unified E4M3 format in DeepSeek-V3":
+ * E4M3 in the backward pass too, and fine-grained quantization strategy).
+ *
+ * x: bf16 [M][K], row stride ldx >= K (ldx % 8 == 0); M % 128 == 0 and K % 128 == 0.
+ * Outputs, bit-identical to fp8_quant_act_1x128 with transposed = 0 and = 1:
+ *     q[M][K], s[M][K/128]   tiles along K;
+ *     qt[K][M], st[K][M/128] tiles along M, stored transposed.
+ * Reads x once (2 bytes per element) instead of twice.
+ * Returns FP8FG_ERR_ARG for a null pointer, misalignment or a shape rule broken.
+ */
+int fp8_quant_act_1x128_dual(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, float *s,
+                             uint8_t *qt, float *st, fp8fg_stream_t stream);
+
+/*
+ * Both orientations of the 128x128 weight quantization from one read of w (same
+ * passages). A 128x128 block holds the same elements, hence the same scale and codes, in
+ * either orientation, so the transposed copy is the B operand of the data-gradient GEMM
+ * dX = dY . W, computed as fp8_blockscaled_gemm(q(dY), s(dY), qt, st, 128x128, ...).
+ *
+ * w: bf16 [N][K], row stride ldw >= K (ldw % 8 == 0); N % 128 == 0 and K % 128 == 0.
+ * Outputs: q[N][K], s[N/128][K/128], bit-identical to fp8_quant_w_128x128, and
+ *     qt[K][N] = q transposed, st[K/128][N/128] = s transposed.
+ * Returns FP8FG_ERR_ARG for a null pointer, misalignment or a shape rule broken.
+ */
+int fp8_quant_w_128x128_dual(const uint16_t *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, float *s,
+                             uint8_t *qt, float *st, fp8fg_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM C = A . B^T ("Advantages of using FP8 for GEMM operations in
  * DeepSeek-V3", items 1, 5 and 8).
  *

@@ -83,6 +83,28 @@ def test_quant_w_argument_errors(lib):
     assert _rc(f, None, 0, 128, 128, None, None, None) == _lib.FP8FG_OK
 
 
+def test_dual_quant_argument_errors(lib):
+    f = lib.fp8_quant_act_1x128_dual
+    ok = (FAKE, 256, 384, 384, FAKE, FAKE, FAKE, FAKE, None)
+
+    def with_(fn, base, i, v):
+        a = list(base)
+        a[i] = v
+        return _rc(fn, *a)
+    assert with_(f, ok, 1, 200) == _lib.FP8FG_ERR_ARG      # M % 128
+    assert with_(f, ok, 2, 200) == _lib.FP8FG_ERR_ARG      # K % 128
+    assert with_(f, ok, 3, 256) == _lib.FP8FG_ERR_ARG      # ldx < K
+    assert with_(f, ok, 3, 388) == _lib.FP8FG_ERR_ARG      # ldx % 8
+    assert with_(f, ok, 6, None) == _lib.FP8FG_ERR_ARG     # null qt
+    assert with_(f, ok, 7, FAKE + 4) == _lib.FP8FG_ERR_ARG  # misaligned st
+    assert with_(f, ok, 1, 0) == _lib.FP8FG_OK             # empty
+    g = lib.fp8_quant_w_128x128_dual
+    assert with_(g, ok, 1, 200) == _lib.FP8FG_ERR_ARG      # N % 128
+    assert with_(g, ok, 2, 136) == _lib.FP8FG_ERR_ARG      # K % 128
+    assert with_(g, ok, 6, None) == _lib.FP8FG_ERR_ARG     # null qt
+    assert with_(g, ok, 2, 0) == _lib.FP8FG_OK             # empty
+
+
 def test_gemm_argument_errors(lib):
     f = lib.fp8_blockscaled_gemm
     ok = (FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 128, 256, 256, None)

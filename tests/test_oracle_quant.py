@@ -182,3 +182,18 @@ def test_quotient_is_a_division_not_a_reciprocal_product():
         codes, scale = quantize_group(tiles[i])
         assert np.float32(scale) == s[i, 0]
         assert q[i].tolist() == codes, i
+
+
+def test_weight_blocks_transpose_symmetric():
+    """A 128x128 block holds the same elements in either orientation, so quantizing W^T
+    gives the transposed codes and scales (the data-gradient operand W^T needs no second
+    quantization); a block index swapped anywhere breaks this on a non-square grid."""
+    rng = np.random.default_rng(12)
+    w = bf16_values(rng.standard_normal((384, 640)) * 0.02)
+    sr = special_rows()
+    w[:128, 128:256] = np.stack([np.roll(sr[i % len(sr)], i) for i in range(128)])
+    w[256:384, 512:640] = 0.0
+    q, s = quant_w_128x128(w)
+    qt, st = quant_w_128x128(np.ascontiguousarray(w.T))
+    assert np.array_equal(qt, q.T) and np.array_equal(st.view(np.uint32), s.T.view(np.uint32))
+    assert st.shape == (5, 3) and s[2, 4] == 0.0
