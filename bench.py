@@ -354,6 +354,20 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                                         "frac": round(fl / t / 1e9 / fp8_peak, 4)}
     del wg, qdy, sdy, qxt, sxt
 
+    # the dense projection with its output kept in FP8 (codes + 1x128 scales)
+    d = inputs.dense(dev)
+    qx, sx = ops.quant_act_1x128(d.x)
+    qw, sw = ops.quant_w_128x128(d.w)
+    del d
+    cq = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    cs = torch.empty((M, N // 128), dtype=torch.float32, device=dev)
+    t = timed(lambda: ops.blockscaled_gemm_e4m3(qx, sx, qw, sw, ops.SB_BLOCK_128x128, out=(cq, cs)), stream, iters,
+              warm, flush)
+    out["blockscaled_gemm dense 4096x18432x7168 e4m3 out"] = {"bound": "tensor", "ms": round(t, 4),
+                                                              "TFLOPs": round(GEMM_FLOPS / t / 1e9, 1),
+                                                              "frac": round(GEMM_FLOPS / t / 1e9 / fp8_peak, 4)}
+    del qx, sx, qw, sw, cq, cs
+
     # both orientations of X from one read (fprop 1x128 along K + wgrad tiles along M)
     xd = inputs.dense(dev, N=128).x                                          # [4096, 7168]
     nb = xd.numel() * 4 + 2 * (xd.numel() // 128) * 4
@@ -521,6 +535,15 @@ def run_case(args):
         del wg
         fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_ROW_1x128, torch.float32)
         work = {"flops": 2.0 * 2048 * 7168 * 4096}
+    elif case == "gemm_e4m3":
+        d = inputs.dense(dev)
+        qx, sx = ops.quant_act_1x128(d.x)
+        qw, sw = ops.quant_w_128x128(d.w)
+        del d
+        cq = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        cs = torch.empty((M, N // 128), dtype=torch.float32, device=dev)
+        fn = lambda: ops.blockscaled_gemm_e4m3(qx, sx, qw, sw, ops.SB_BLOCK_128x128, out=(cq, cs))
+        work = {"flops": GEMM_FLOPS}
     elif case == "qdual":
         x = inputs.dense(dev, N=128).x
         fn = lambda: ops.quant_act_1x128_dual(x)
@@ -574,7 +597,7 @@ def main():
     ap.add_argument("--cpu-sample-wrows", type=int, default=4608)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--ref-wrows", type=int, default=2048)
-    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad"],
+    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad", "gemm_e4m3"],
                     help="time one kernel on its workload instead of the step (for profiling)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()

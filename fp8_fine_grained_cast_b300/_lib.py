@@ -42,6 +42,7 @@ SIGNATURES = {
     "fp8_quant_act_1x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_quant_w_128x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_blockscaled_gemm": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P]),
+    "fp8_blockscaled_gemm_e4m3": (_I, [_P, _P, _P, _P, _I, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _P, _I, _I64, _I64, _P]),
     "fp8fg_last_error": (ctypes.c_char_p, []),
     "fp8fg_sync_status": (_I, [_P]),
@@ -107,6 +108,10 @@ def fp8_quant_w_128x128_dual(w, N, K, ldw, q, s, qt, st, stream):
 
 def fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):
     return _check(lib().fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream))
+
+
+def fp8_blockscaled_gemm_e4m3(qa, sa, qb, sb, sb_kind, c_q, c_s, M, N, K, stream):
+    return _check(lib().fp8_blockscaled_gemm_e4m3(qa, sa, qb, sb, sb_kind, c_q, c_s, M, N, K, stream))
 
 
 def fp8_grouped_gemm(qa, sa, qb, sb, group_offsets, E, Mtot, c, c_dtype, N, K, stream):

@@ -174,7 +174,36 @@ int fp8_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, 
   if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: pointers must be 16-byte aligned");
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
-  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype == FP8FG_OUT_BF16, M, N, K,
+  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, nullptr,
+                                                         c_dtype == FP8FG_OUT_BF16 ? 1 : 0, M, N, K,
+                                                         reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
+  if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
+  return FP8FG_OK;
+}
+
+int fp8_blockscaled_gemm_e4m3(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,
+                              uint8_t* c_q, float* c_s, int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: negative size");
+  if (sb_kind != FP8FG_SB_BLOCK_128x128 && sb_kind != FP8FG_SB_ROW_1x128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: unknown sb_kind %d", sb_kind);
+  if (K % 128 || N % 128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: K=%lld and N=%lld must be multiples of 128", (long long)K, (long long)N);
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: dimension too large");
+  if (M == 0 || N == 0) return FP8FG_OK;
+  if (!c_q || !c_s) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: null output pointer");
+  if (!aligned16(c_q) || !aligned16(c_s)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: pointers must be 16-byte aligned");
+  if (K == 0) {  // C = 0: every tile is all-zero, scale +0 and codes 0x00
+    DeviceInfo dev;
+    if (int rc = current_device(&dev)) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemsetAsync(c_q, 0, static_cast<size_t>(M) * N, st);
+    if (err == cudaSuccess) err = cudaMemsetAsync(c_s, 0, static_cast<size_t>(M) * (N / 128) * sizeof(float), st);
+    return err == cudaSuccess ? FP8FG_OK : cuda_fail(err, "cudaMemsetAsync");
+  }
+  if (!qa || !sa || !qb || !sb) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: null pointer");
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_e4m3: pointers must be 16-byte aligned");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c_q, c_s, 2, M, N, K,
                                                          reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
   if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
   return FP8FG_OK;

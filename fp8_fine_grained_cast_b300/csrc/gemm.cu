@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "internal.h"
 
 namespace fp8fg {
@@ -75,7 +76,7 @@ struct WarpLayout {
   static constexpr uint32_t kTmemCols = 2 * kTmemBuf;
 };
 
-template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
+template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
 struct GemmCfg : WarpLayout<BN> {
   using L = WarpLayout<BN>;
   static constexpr int kStageA = kBM * kBK;
@@ -96,7 +97,9 @@ struct GemmCfg : WarpLayout<BN> {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffsets = kOffMisc + 16;
   static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
-  static constexpr int kBoxCols = OUT_BF16 ? 64 : 32;  // epilogue box: 32 rows x 128 bytes
+  // epilogue box: 32 rows x 128 bytes of FP32 (OUT 0), BF16 (OUT 1) or E4M3 codes (OUT 2)
+  static constexpr int kBoxCols = OUT == 0 ? 32 : OUT == 1 ? 64 : 128;
+  static_assert(OUT != 2 || L::kCols == 128, "an E4M3 output row slice is one 1x128 tile");
   static_assert(L::kCols % kBoxCols == 0, "epilogue boxes");
 };
 
@@ -191,13 +194,13 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
   }
 }
 
-template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
+template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
 __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                            void* __restrict__ c_out, const float* __restrict__ sa,
+                            void* __restrict__ c_out, float* __restrict__ c_scale, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
                             int K, int num_m_tiles, int num_n_tiles) {
-  using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
+  using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
   constexpr int kPromoWarps = Cfg::kPromoWarps;
   constexpr int kGroup = kSlots / 2;   // chunks per scale-loader group (two groups in flight)
@@ -487,9 +490,23 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         // banks), then the warp reads it back four rows per instruction and stores
         // four full 128-byte lines per instruction to C. The stores go through the
         // load/store path, not the TMA unit, which is busy with the operand loads.
+        // E4M3 output (OUT 2): this thread's 128 columns of row m0 + row are one 1x128
+        // tile of C, quantized like an activation tile (scale fl32(amax / 448), codes
+        // E4M3(fl32(c / s))) straight from the FP32 accumulators.
         constexpr int kBoxCols = Cfg::kBoxCols;
         uint8_t* c_bytes = reinterpret_cast<uint8_t*>(c_out);
-        constexpr int kEsize = OUT_BF16 ? 2 : 4;
+        constexpr int kEsize = OUT == 0 ? 4 : OUT == 1 ? 2 : 1;
+        Scale osc;
+        if constexpr (OUT == 2) {
+          float am0 = 0.0f, am1 = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kCols; i += 2) {
+            am0 = fmaxf(am0, fabsf(acc[i]));
+            am1 = fmaxf(am1, fabsf(acc[i + 1]));
+          }
+          osc = make_scale(fmaxf(am0, am1));
+          if (col0 < N && m0 + row < M) c_scale[static_cast<int64_t>(m0 + row) * (N / 128) + col0 / 128] = osc.s;
+        }
 #pragma unroll
         for (int h = 0; h < kCols / kBoxCols; ++h) {
           const int box_col = col0 + h * kBoxCols;
@@ -497,7 +514,11 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             uint4 w;
-            if constexpr (OUT_BF16) {
+            if constexpr (OUT == 2) {
+              const float* a = acc + 16 * ch;
+              w = make_uint4(quantize4(a[0], a[1], a[2], a[3], osc), quantize4(a[4], a[5], a[6], a[7], osc),
+                             quantize4(a[8], a[9], a[10], a[11], osc), quantize4(a[12], a[13], a[14], a[15], osc));
+            } else if constexpr (OUT == 1) {
               const float* a = acc + h * 64 + 8 * ch;
               w = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                              pack_bf16x2(a[6], a[7]));
@@ -535,12 +556,12 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <int BN, int STAGES, int SB_KIND, bool OUT_BF16, bool GROUPED>
+template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
 LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                       const int32_t* offsets, int E, int64_t M, int64_t N, int64_t K, int64_t b_rows, void* c,
-                      cudaStream_t stream, int sm_count) {
-  using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, SB_KIND, OUT_BF16, GROUPED>;
+                      float* c_scale, cudaStream_t stream, int sm_count) {
+  using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, SB_KIND, OUT, GROUPED>;
   const size_t smem = Cfg::smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return {err, "cudaFuncSetAttribute(max dynamic shared memory)"};
@@ -561,7 +582,7 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   const int num_n = static_cast<int>((N + BN - 1) / BN);
   const int64_t tiles = static_cast<int64_t>(num_m) * num_n;
   const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
-  kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, sa, sb, offsets, E, static_cast<int>(M),
+  kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, c_scale, sa, sb, offsets, E, static_cast<int>(M),
                                            static_cast<int>(N), static_cast<int>(K), num_m, num_n);
   err = cudaGetLastError();
   if (err != cudaSuccess) return {err, "kernel launch"};
@@ -571,25 +592,27 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 }  // namespace
 
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
-                                     int sb_kind, void* c, int c_bf16, int64_t M, int64_t N, int64_t K,
-                                     cudaStream_t stream, int sm_count) {
+                                     int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
+                                     int64_t K, cudaStream_t stream, int sm_count) {
   // 128 x 256 tiles throughout: 128-column tiles, tried for the weight-gradient shape
   // whose 256-column tiles leave a nearly empty last wave, measured slower (the fixed
   // per-chunk cost of the promotion handshake is paid twice as often).
   if (sb_kind == 0) {
-    if (c_bf16) return run_gemm<256, 4, 0, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-    return run_gemm<256, 4, 0, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+    if (c_kind == 1) return run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+    if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
+    return run_gemm<256, 4, 0, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
   }
-  if (c_bf16) return run_gemm<256, 3, 1, true, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
-  return run_gemm<256, 3, 1, false, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, stream, sm_count);
+  if (c_kind == 1) return run_gemm<256, 3, 1, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+  if (c_kind == 2) return run_gemm<256, 3, 1, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
+  return run_gemm<256, 3, 1, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
 }
 
 LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                  const int32_t* offsets, int E, int64_t Mtot, void* c, int c_bf16, int64_t N,
                                  int64_t K, cudaStream_t stream, int sm_count) {
   if (c_bf16)
-    return run_gemm<256, 3, 0, true, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, stream, sm_count);
-  return run_gemm<256, 3, 0, false, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, stream, sm_count);
+    return run_gemm<256, 3, 0, 1, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, nullptr, stream, sm_count);
+  return run_gemm<256, 3, 0, 0, true>(qa, sa, qb, sb, offsets, E, Mtot, N, K, N * E, c, nullptr, stream, sm_count);
 }
 
 namespace {

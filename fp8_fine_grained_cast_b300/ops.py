@@ -122,6 +122,27 @@ def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out_dtype=
     return c
 
 
+def blockscaled_gemm_e4m3(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out=None):
+    """C = A . B^T quantized in 1x128 tiles from the FP32 accumulators:
+    returns (c_q uint8 [M, N], c_s float32 [M, N/128])."""
+    for t, n, dt, nd in ((qa, "qa", torch.uint8, 2), (sa, "sa", torch.float32, 2), (qb, "qb", torch.uint8, 2),
+                         (sb, "sb", torch.float32, 2)):
+        _need(t, dt, n, nd)
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    M, K = qa.shape
+    N = qb.shape[0]
+    if qb.shape[1] != K:
+        raise ValueError("qa and qb disagree on K")
+    if out is None:
+        out = (torch.empty((M, N), dtype=torch.uint8, device=qa.device),
+               torch.empty((M, N // 128), dtype=torch.float32, device=qa.device))
+    c_q, c_s = out
+    _lib.fp8_blockscaled_gemm_e4m3(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), sb_kind,
+                                   c_q.data_ptr(), c_s.data_ptr(), M, N, K, _stream())
+    return c_q, c_s
+
+
 def grouped_gemm(qa, sa, qb, sb, group_offsets, out_dtype=torch.bfloat16, c=None):
     """Grouped GEMM: qa [Mtot, K], qb [E, N, K], sb [E, N/128, K/128], offsets int32 [E+1]."""
     _need(qa, torch.uint8, "qa", 2)

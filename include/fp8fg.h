@@ -142,6 +142,25 @@ int fp8_blockscaled_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, 
                          fp8fg_stream_t stream);
 
 /*
+ * Block-scaled FP8 GEMM whose output is quantized to E4M3 in 1x128 tiles (activations
+ * kept in FP8 between layers: "Unified E4M3 format in DeepSeek-V3", memory section; the
+ * quantization is the one of fp8_quant_act_1x128).
+ *
+ * C = A . B^T is formed exactly as by fp8_blockscaled_gemm (same operands, layouts and
+ * per-chunk FP32 promotion); then every 1x128 tile of C (row m, columns 128 t .. 128 t
+ * + 127) is quantized from the FP32 accumulators, without rounding to BF16 first:
+ *     c_s[m][t] = fl32(max |C| over the tile / 448),
+ *     c_q[m][n] = E4M3FN(fl32(C[m][n] / c_s[m][n / 128])), RNE, saturating;
+ *     an all-zero tile gets scale +0 and codes 0x00.
+ * c_q: [M][N] uint8 (row stride N), c_s: [M][N/128] float; (c_q, c_s) can be the A
+ * operand of a following GEMM. Requires K % 128 == 0 and N % 128 == 0; any M >= 0.
+ * K == 0 gives C = 0: all scales +0 and all codes 0x00.
+ */
+int fp8_blockscaled_gemm_e4m3(const uint8_t *qa, const float *sa, const uint8_t *qb, const float *sb,
+                              int sb_kind, uint8_t *c_q, float *c_s, int64_t M, int64_t N, int64_t K,
+                              fp8fg_stream_t stream);
+
+/*
  * Grouped (MoE expert) block-scaled FP8 GEMM ("Advantages of using FP8 for GEMM
  * operations in DeepSeek-V3", item 8: the MoE variant).
  *

@@ -33,7 +33,11 @@ Readings where the pages are silent (each also listed in the design notes):
 * the GEMM result is C[m,n] = sum_k dec(qa[m,k]) sa[m,k/128] dec(qb[n,k]) sb(n,k),
   accumulated in float64 (the FP32 promotion of the pages reaches the same value up
   to fp32 rounding); C = A . B^T with both operands K-contiguous;
-* the grouped GEMM is the dense GEMM applied to each expert's contiguous rows.
+* the grouped GEMM is the dense GEMM applied to each expert's contiguous rows;
+* a GEMM whose output stays in FP8 (the Arabic page's memory section: activations
+  stored in FP8) quantizes its FP32 result in 1x128 tiles along N with the activation
+  quantizer, without rounding to BF16 first; the oracle's FP32 result is the float64
+  sum rounded once to binary32.
 
 E4M3FN is the OCP 8-bit floating point format "E4M3": bit layout s.eeee.mmm,
 exponent bias 7, subnormals at e = 0 (value m * 2^-9), no infinities, NaN only at
@@ -110,7 +114,7 @@ def e4m3_encode(y: np.ndarray) -> np.ndarray:
 
 
 def _quantize_groups(g: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    """Quantize groups laid out as g[..., group_elements] (float32, bf16-valued).
+    """Quantize groups laid out as g[..., group_elements] (float32 values).
 
     Per group: amax = max |x| (exact), s = fl32(amax / 448), q = E4M3(fl32(x / s)).
     A group with amax == 0 gets s = 0 and codes 0x00.
@@ -129,7 +133,7 @@ def _quantize_groups(g: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
 def quant_act_1x128(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     """Activation quantization in 1x128 tiles along the last (K) dimension.
 
-    x: float32 [M, K] holding bf16 values, K % 128 == 0.
+    x: float32 [M, K] (bf16 values for activations; any binary32 values work), K % 128 == 0.
     Returns q uint8 [M, K] (E4M3FN codes) and s float32 [M, K/128], s[m, t] being the
     scale of columns 128t .. 128t+127 of row m; x[m, k] ~= dec(q[m, k]) * s[m, k // 128].
     Follows the Russian page, item 1, and the Arabic page, "fine-grained strategy".
@@ -222,6 +226,19 @@ def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, rows=None)
     A = dequant_rows_1x128(qa, sa)
     B = dequant_b(np.asarray(qb), np.asarray(sb), sb_kind)
     return A @ B.T
+
+
+def blockscaled_gemm_e4m3(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, rows=None):
+    """The block-scaled GEMM with its output quantized in 1x128 tiles along N.
+
+    C = blockscaled_gemm(...) (float64) is rounded once to binary32 and quantized by
+    quant_act_1x128: returns (codes uint8 [M, N], scales float32 [M, N/128], C32).
+    Follows the Arabic page, memory section (activations kept in FP8), with the
+    quantization of the Russian page, item 1.
+    """
+    c32 = blockscaled_gemm(qa, sa, qb, sb, sb_kind, rows=rows).astype(np.float32)
+    q, s = quant_act_1x128(c32)
+    return q, s, c32
 
 
 def grouped_gemm(qa, sa, qb, sb, group_offsets, experts=None) -> np.ndarray:

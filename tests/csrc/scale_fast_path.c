@@ -8,6 +8,9 @@
  *   r  = RN(1 / s)       as  y1 = fma(y0, fma(-s, y0, 1), y0); r = fma(y1, fma(-s, y1, 1), y1)
  *        from a hardware approximation y0 of 1 / s (one Newton-Raphson step, then
  *        Markstein's correction step for the reciprocal).
+ * The correction step for the reciprocal is known to miss when the significand of s is
+ * all ones; the kernels then divide instead, and this program checks that it is the only
+ * significand that misses (it skips the reciprocal for it and counts the skips).
  * The hardware approximation is documented to be within one unit in the last place;
  * this program tries every y0 within SPREAD units of the correctly rounded 1 / s, so
  * the check does not depend on which approximation the hardware returns.
@@ -15,7 +18,10 @@
  * binary64 (the products involved have at most 48 significant bits):
  *   s is RN(amax / 448) iff |amax - 448 s| < 224 ulp(s), or = with an even s;
  *   r is RN(1 / s)      iff |1 - s r| < s ulp(r) / 2, or = with an even r.
- * Every positive finite bf16 value in the range is an amax the kernels can meet.
+ * Every positive finite bf16 value in the range is an amax the kernels can meet; the GEMM
+ * epilogue also meets binary32 values, for which every significand is checked in
+ * [1, 4): inside the range every step above (and its exactness or rounding) scales with
+ * powers of two, so one binade of amax covers all, and its scales fill a binade of s.
  * Prints "values_checked mismatches"; exit status 1 on any mismatch.
  */
 #include <math.h>
@@ -42,36 +48,49 @@ static int is_rn_reciprocal(float s, float r) {
     return d < h || (d == h && (to_bits(r) & 1u) == 0);
 }
 
-int main(void) {
+/* Checks one amax; adds to the counters. */
+static void check(float amax, unsigned long long *checked, unsigned long long *bad) {
     const float c = 1.0f / 448.0f;
+    const float q0 = amax * c;
+    const float e = fmaf(-q0, 448.0f, amax);
+    const float s = fmaf(e, c, q0);
+    ++*checked;
+    if (!is_rn_quotient(amax, s) || s != amax / 448.0f) {
+        if (*bad < 10) fprintf(stderr, "scale: amax %a s %a want %a\n", amax, s, amax / 448.0f);
+        ++*bad;
+        return;
+    }
+    if ((to_bits(s) & 0x7FFFFFu) == 0x7FFFFFu) return;   /* divided by the kernels */
+    const float want = 1.0f / s;
+    if (!is_rn_reciprocal(s, want)) {
+        fprintf(stderr, "reference reciprocal check failed for s %a\n", s);
+        ++*bad;
+    }
+    for (int k = -SPREAD; k <= SPREAD; ++k) {
+        const float y0 = from_bits(to_bits(want) + (uint32_t)k);
+        const float y1 = fmaf(y0, fmaf(-s, y0, 1.0f), y0);
+        const float r = fmaf(y1, fmaf(-s, y1, 1.0f), y1);
+        ++*checked;
+        if (r != want) {
+            if (*bad < 10) fprintf(stderr, "reciprocal: s %a y0 %a got %a want %a\n", s, y0, r, want);
+            ++*bad;
+        }
+    }
+}
+
+int main(void) {
     unsigned long long checked = 0, bad = 0;
     for (uint32_t ab = 0x0001; ab < 0x7F80; ++ab) {
         const float amax = from_bits(ab << 16);
         if (!(amax >= 0x1p-70f && amax <= 0x1p+108f)) continue;
-        const float q0 = amax * c;
-        const float e = fmaf(-q0, 448.0f, amax);
-        const float s = fmaf(e, c, q0);
-        ++checked;
-        if (!is_rn_quotient(amax, s) || s != amax / 448.0f) {
-            if (bad < 10) fprintf(stderr, "scale: amax %a s %a want %a\n", amax, s, amax / 448.0f);
-            ++bad;
-            continue;
-        }
-        const float want = 1.0f / s;
-        if (!is_rn_reciprocal(s, want)) {
-            fprintf(stderr, "reference reciprocal check failed for s %a\n", s);
-            ++bad;
-        }
-        for (int k = -SPREAD; k <= SPREAD; ++k) {
-            const float y0 = from_bits(to_bits(want) + (uint32_t)k);
-            const float y1 = fmaf(y0, fmaf(-s, y0, 1.0f), y0);
-            const float r = fmaf(y1, fmaf(-s, y1, 1.0f), y1);
-            ++checked;
-            if (r != want) {
-                if (bad < 10) fprintf(stderr, "reciprocal: s %a y0 %a got %a want %a\n", s, y0, r, want);
-                ++bad;
-            }
-        }
+        check(amax, &checked, &bad);
+    }
+#pragma omp parallel for schedule(static) reduction(+ : checked, bad)
+    for (uint32_t u = 0x3F800000u; u < 0x40800000u; ++u) {   /* every binary32 in [1, 4) */
+        unsigned long long c = 0, b = 0;
+        check(from_bits(u), &c, &b);
+        checked += c;
+        bad += b;
     }
     printf("%llu %llu\n", checked, bad);
     return bad != 0;

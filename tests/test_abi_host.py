@@ -123,6 +123,22 @@ def test_gemm_argument_errors(lib):
     assert with_(7, 0) == _lib.FP8FG_OK                 # empty
 
 
+def test_gemm_e4m3_argument_errors(lib):
+    f = lib.fp8_blockscaled_gemm_e4m3
+    ok = (FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, 128, 256, 256, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return _rc(f, *a)
+    assert with_(4, 3) == _lib.FP8FG_ERR_ARG            # sb_kind
+    assert with_(8, 200) == _lib.FP8FG_ERR_ARG          # N % 128
+    assert with_(9, 100) == _lib.FP8FG_ERR_ARG          # K % 128
+    assert with_(6, None) == _lib.FP8FG_ERR_ARG         # null scale output
+    assert with_(5, FAKE + 8) == _lib.FP8FG_ERR_ARG     # misaligned codes
+    assert with_(7, 0) == _lib.FP8FG_OK                 # empty
+
+
 def test_grouped_argument_errors(lib):
     f = lib.fp8_grouped_gemm
     ok = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 512, FAKE, 1, 256, 256, None]

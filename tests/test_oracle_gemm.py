@@ -137,3 +137,53 @@ def test_relative_error_measure():
     assert relative_error(ref + np.array([[0.0, 0.0], [0.0, 0.25]]), ref) == 0.25 / 4.0
     assert relative_error(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
     assert relative_error(np.ones(2), np.zeros(2)) == float("inf")
+
+
+def test_gemm_e4m3_output_closed_form():
+    """A = ones (code 0x38, scale 1), K = 128, B row n constant with value v_n, so
+    C[m, n] = 128 v_n sb_n exactly; with v_n = k n / 8 patterns the tile maxima and
+    quotients are known rationals and the codes are checked against the exact
+    restatement (rational arithmetic, nearest E4M3 value by table search).
+    v_n = ((n mod 13) - 6) / 2 are E4M3 values (at most 3 significant bits)."""
+    from oracle.fp8_oracle import blockscaled_gemm_e4m3, e4m3_encode
+    from tests.exact_ref import quantize_group
+    M, N, K = 3, 256, 128
+    qa = np.full((M, K), 0x38, np.uint8)
+    sa = np.ones((M, 1), np.float32)
+    vals = np.array([((n % 13) - 6) / 2.0 for n in range(N)], np.float32)
+    codes = e4m3_encode(vals)
+    qb = np.repeat(codes[:, None], K, axis=1)
+    sb = np.array([[0.5], [4.0]], np.float32)                                 # 128x128 blocks of B
+    q, s, c32 = blockscaled_gemm_e4m3(qa, sa, qb, sb)
+    dec = np.array([float(v) for v in vals])
+    for n in range(N):
+        assert c32[0, n] == np.float32(128.0 * dec[n] * sb[n // 128, 0])
+    for t in range(2):
+        want_codes, want_s = quantize_group(c32[1, 128 * t:128 * t + 128])
+        assert np.float32(want_s) == s[1, t]
+        assert q[1, 128 * t:128 * t + 128].tolist() == want_codes
+    # the tile maximum |C| = 128 * 3 * sb sets the scale, and its elements encode to +-448
+    assert s[0, 0] == np.float32(128 * 3 * 0.5 / 448) and s[0, 1] == np.float32(128 * 3 * 4.0 / 448)
+    assert set(q[0][np.abs(c32[0]) == np.abs(c32[0]).max()].tolist()) <= {0x7E, 0xFE}
+
+
+def test_quantizer_on_binary32_values_matches_exact_restatement():
+    """The GEMM epilogue quantizes FP32 (not bf16) values: tiles of random binary32
+    values, values placed on and next to E4M3 rounding midpoints of x / s, signed zeros
+    and tiny magnitudes, against the exact rational restatement."""
+    from oracle.fp8_oracle import quant_act_1x128
+    from tests.exact_ref import quantize_group
+    rng = np.random.default_rng(21)
+    rows = [rng.standard_normal(128).astype(np.float32) * np.float32(3.7)]
+    r = rng.standard_normal(128).astype(np.float32); r[0] = np.float32(448.0)   # s = 1: midpoints exact
+    r[1:20] = np.float32(1.0625); r[20:40] = np.nextafter(np.float32(1.0625), np.float32(2)); r[40] = -0.0
+    r[41] = np.float32(-2 ** -10); r[42] = np.float32(2 ** -10); r[43] = np.float32(3 * 2 ** -11)
+    rows.append(r)
+    rows.append((rng.random(128) * 1e-30).astype(np.float32))
+    rows.append((rng.standard_normal(128) * 1e20).astype(np.float32))
+    x = np.array(rows, np.float32)
+    q, s = quant_act_1x128(x)
+    for m in range(x.shape[0]):
+        codes, scale = quantize_group(x[m])
+        assert np.float32(scale) == s[m, 0]
+        assert q[m].tolist() == codes, m
