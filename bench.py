@@ -336,6 +336,37 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                           "frac": round(nb / t / 1e6 / hbm_peak, 4), "algorithmic_bytes": nb}
     del xq
 
+    # delayed (history) scaling on the same tensor, and its accuracy contrast with online
+    # 1x128 scaling when the data grow by 1.5x over the recorded maxima
+    xq = inputs.quant_only(dev)
+    hist = ops.new_amax_history(16, dev)
+    amax0 = xq.abs().max().float()
+    hist[:16] = amax0
+    nb = xq.numel() * 3 + xq.numel() // 128 * 4
+
+    def delayed_step():
+        ops.quant_act_delayed(xq, hist)
+        hist[:16] = amax0                        # keep the recorded maxima fixed between runs
+    t = timed(delayed_step, stream, iters, warm, flush)
+    x2 = (xq.float() * 1.5).to(torch.bfloat16)
+    qd, sd = ops.quant_act_delayed(x2, hist)
+    qo, so = ops.quant_act_1x128(x2)
+    ref = x2.float()
+
+    def deq(q, sc):
+        return q.view(torch.float8_e4m3fn).float() * sc.repeat_interleave(128, dim=1)
+    err_d = ((deq(qd, sd) - ref).abs().sum() / ref.abs().sum()).item()
+    err_o = ((deq(qo, so) - ref).abs().sum() / ref.abs().sum()).item()
+    # values beyond 448 s are clipped to +-448 s (online scaling clips nothing by construction)
+    clip_d = (ref.abs() > 448.0 * sd.repeat_interleave(128, dim=1)).float().mean().item()
+    clip_o = (ref.abs() > 448.0 * so.repeat_interleave(128, dim=1)).float().mean().item()
+    out["quant_act_delayed [16384,7168] H16"] = {
+        "bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1), "frac": round(nb / t / 1e6 / hbm_peak, 4),
+        "algorithmic_bytes": nb,
+        "contrast_x1.5_growth": {"rel_l1_err_delayed": round(err_d, 5), "rel_l1_err_online": round(err_o, 5),
+                                 "clipped_frac_delayed": round(clip_d, 7), "clipped_frac_online": round(clip_o, 7)}}
+    del xq, x2, qd, sd, qo, so, ref
+
     wg = inputs.wgrad(dev)
     for name, tsr in (("dY [4096,2048]", wg.dy), ("X [4096,7168]", wg.x)):
         nb = tsr.numel() * 3 + tsr.numel() // 128 * 4
@@ -544,6 +575,12 @@ def run_case(args):
         cs = torch.empty((M, N // 128), dtype=torch.float32, device=dev)
         fn = lambda: ops.blockscaled_gemm_e4m3(qx, sx, qw, sw, ops.SB_BLOCK_128x128, out=(cq, cs))
         work = {"flops": GEMM_FLOPS}
+    elif case == "qdelayed":
+        x = inputs.quant_only(dev)
+        hist = ops.new_amax_history(16, dev)
+        hist[:16] = x.abs().max().float()
+        fn = lambda: ops.quant_act_delayed(x, hist)
+        work = {"bytes": x.numel() * 3 + x.numel() // 128 * 4}
     elif case == "qdual":
         x = inputs.dense(dev, N=128).x
         fn = lambda: ops.quant_act_1x128_dual(x)
@@ -597,7 +634,7 @@ def main():
     ap.add_argument("--cpu-sample-wrows", type=int, default=4608)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--ref-wrows", type=int, default=2048)
-    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad", "gemm_e4m3"],
+    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad", "gemm_e4m3", "qdelayed"],
                     help="time one kernel on its workload instead of the step (for profiling)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()

@@ -96,6 +96,34 @@ int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, in
   return FP8FG_OK;
 }
 
+int fp8_quant_act_delayed(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* amax_history, int H,
+                          uint8_t* q, float* s, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (M < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: negative size");
+  if (K % 128) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: K=%lld is not a multiple of 128", (long long)K);
+  if (ldx < K || ldx % 8) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: ldx=%lld must be >= K and a multiple of 8", (long long)ldx);
+  if (H < 1 || H > 1024) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: history length %d outside 1..1024", H);
+  if (M > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: dimension too large");
+  if (!amax_history) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: null history");
+  if (!aligned16(amax_history)) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: pointers must be 16-byte aligned");
+  if (M > 0 && K > 0) {
+    if (!x || !q || !s) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: null pointer");
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return fail(FP8FG_ERR_ARG, "fp8_quant_act_delayed: pointers must be 16-byte aligned");
+  }
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaError_t err;
+  if (M == 0 || K == 0) {  // nothing to quantize: max |x| = 0 still enters the history
+    err = fp8fg::launch_quant_act_delayed(nullptr, 0, 128, 128, amax_history, H, nullptr, nullptr,
+                                          reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
+  } else {
+    err = fp8fg::launch_quant_act_delayed(x, M, K, ldx, amax_history, H, q, s, reinterpret_cast<cudaStream_t>(stream),
+                                          dev.sm_count);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_act_delayed launch");
+  return FP8FG_OK;
+}
+
 int fp8_quant_w_128x128(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, float* s,
                         fp8fg_stream_t stream) {
   g_last_error[0] = '\0';

@@ -16,6 +16,10 @@ cudaError_t launch_quant_act_cols(const uint16_t* x, int64_t M, int64_t K, int64
 // qt[K][M], st[K][M/128] (tiles along M); M and K multiples of 128.
 cudaError_t launch_quant_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
                                   uint8_t* qt, float* st, cudaStream_t stream, int sm_count);
+// Delayed scaling: one scale from history[0..H-1], history[H] the max |x| accumulator
+// (zero on entry and on return); pushes this call's max |x| into the history.
+cudaError_t launch_quant_act_delayed(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* history, int H,
+                                     uint8_t* q, float* s, cudaStream_t stream, int sm_count);
 // 2D row-major tensor [rows][cols] with the given row pitch in bytes; box = box_cols x
 // box_rows elements; optional 128-byte swizzle; out-of-range elements read as zero.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t cols, uint64_t rows,

@@ -55,6 +55,27 @@ def quant_act_1x128(x: torch.Tensor, transposed: bool = False, q=None, s=None):
     return q, s
 
 
+def new_amax_history(H: int, device) -> torch.Tensor:
+    """Zero-initialized history state for quant_act_delayed: float32 [H + 1]."""
+    return torch.zeros(H + 1, dtype=torch.float32, device=device)
+
+
+def quant_act_delayed(x: torch.Tensor, amax_history: torch.Tensor, q=None, s=None):
+    """Delayed scaling of x bf16 [M, K] with the per-tensor scale from amax_history
+    (float32 [H + 1], updated in place): returns (q uint8 [M, K], s float32 [M, K/128])."""
+    _need(x, torch.bfloat16, "x", 2)
+    _rows_contiguous(x, "x")
+    _need(amax_history, torch.float32, "amax_history", 1)
+    if not amax_history.is_contiguous():
+        raise ValueError("amax_history must be contiguous")
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    s = torch.empty((M, K // 128), dtype=torch.float32, device=x.device) if s is None else s
+    _lib.fp8_quant_act_delayed(x.data_ptr(), M, K, x.stride(0), amax_history.data_ptr(), amax_history.numel() - 1,
+                               q.data_ptr(), s.data_ptr(), _stream())
+    return q, s
+
+
 def quant_w_128x128(w: torch.Tensor, q=None, s=None):
     """w bf16 [N, K] -> (q uint8 [N, K], s float32 [N/128, K/128])."""
     _need(w, torch.bfloat16, "w", 2)

@@ -87,6 +87,30 @@ int fp8_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, in
                         uint8_t *q, float *s, fp8fg_stream_t stream);
 
 /*
+ * Delayed (history-based) quantization, the contrast to the online scaling above
+ * ("Online quantization vs delayed quantization in DeepSeek-V3", items 2-3: delayed
+ * quantization derives the scale from maximum values recorded in earlier iterations
+ * and has to keep that history).
+ *
+ * x: bf16 [M][K], row stride ldx >= K (ldx % 8 == 0); K % 128 == 0; any M >= 0.
+ * amax_history: DEVICE float [H + 1], 1 <= H <= 1024, caller-owned state that lives
+ *     across calls: entries 0..H-1 are the per-tensor maxima max |x| of the H most
+ *     recent calls, most recent first; entry H must be +0 (the library leaves it +0).
+ *     Zero-initialize all H + 1 floats before the first call.
+ * One scale for the whole tensor: s = fl32(max(amax_history[0..H-1]) / 448), or s = 1
+ * when that maximum is 0 (no history yet). Codes q[M][K] = E4M3FN(fl32(x / s)),
+ * saturating to +-448 (values beyond 448 s saturate; online scaling never does), and
+ * s[M][K/128] = s for every 1x128 tile, so (q, s) can be the A operand of
+ * fp8_blockscaled_gemm. Then the history shifts by one: amax_history[0] = max |x| of
+ * this call (exact), the oldest entry drops out.
+ * Two kernels on `stream`: the quantization (which also accumulates max |x| into entry
+ * H) and a one-block history update. Calls that share a history must be ordered.
+ * Returns FP8FG_ERR_ARG for a null pointer, misalignment or a shape rule broken.
+ */
+int fp8_quant_act_delayed(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, float *amax_history, int H,
+                          uint8_t *q, float *s, fp8fg_stream_t stream);
+
+/*
  * Weight quantization in 128x128 blocks (same passages as above).
  *
  * w: bf16 [N][K], row stride ldw >= K (ldw % 8 == 0); N % 128 == 0, K % 128 == 0.

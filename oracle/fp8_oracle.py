@@ -34,6 +34,10 @@ Readings where the pages are silent (each also listed in the design notes):
   accumulated in float64 (the FP32 promotion of the pages reaches the same value up
   to fp32 rounding); C = A . B^T with both operands K-contiguous;
 * the grouped GEMM is the dense GEMM applied to each expert's contiguous rows;
+* delayed scaling (the contrast of the Russian page, items 2-3) keeps one scale per
+  tensor from the maxima of earlier calls: s = fl32(max(history) / 448), s = 1 for an
+  empty history, codes E4M3(fl32(x / s)) saturating, and this call's max |x| enters
+  the history;
 * a GEMM whose output stays in FP8 (the Arabic page's memory section: activations
   stored in FP8) quantizes its FP32 result in 1x128 tiles along N with the activation
   quantizer, without rounding to BF16 first; the oracle's FP32 result is the float64
@@ -161,6 +165,36 @@ def quant_act_1x128_transposed(x: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     if x.shape[0] % TILE:
         raise ValueError("T must be a multiple of 128")
     return quant_act_1x128(np.ascontiguousarray(x.T))
+
+
+def quant_act_delayed(x: np.ndarray, history: np.ndarray):
+    """Delayed (history-based) scaling of a tensor, the contrast to online scaling.
+
+    x: float32 [M, K] (bf16 values), K % 128 == 0; history: float32 [H], the per-tensor
+    maxima of the H previous calls, most recent first.
+    s = fl32(max(history) / 448), or 1 when that maximum is 0; q = E4M3(fl32(x / s)),
+    saturating (a quotient beyond the binary32 range is infinite and saturates too).
+    Returns q uint8 [M, K], the tile scales float32 [M, K/128] (all equal to s) and the
+    new history [H]: max |x| first, the oldest entry dropped.
+    Follows the Russian page, items 2-3 (delayed quantization relies on historical
+    maxima that have to be stored).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    history = np.asarray(history, dtype=np.float32)
+    M, K = x.shape
+    if K % TILE:
+        raise ValueError("K must be a multiple of 128")
+    hmax = np.float32(history.max()) if history.size else np.float32(0.0)
+    s = (hmax / np.float32(E4M3_MAX)).astype(np.float32) if hmax > 0 else np.float32(1.0)
+    with np.errstate(over="ignore"):
+        y = (x / s).astype(np.float32)                            # IEEE binary32 division
+    # an infinite quotient lies beyond 448 like any other overflowing one: saturate it
+    y = np.where(np.isinf(y), np.copysign(np.float32(2 * E4M3_MAX), y), y).astype(np.float32)
+    q = e4m3_encode(y)
+    tiles = np.full((M, K // TILE), s, np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    new_history = np.concatenate([[amax], history[:-1]]).astype(np.float32)
+    return q, tiles, new_history
 
 
 def quant_w_128x128(w: np.ndarray) -> tuple[np.ndarray, np.ndarray]:

@@ -74,6 +74,22 @@ def test_quant_act_argument_errors(lib):
     assert lib.fp8fg_last_error() == b""
 
 
+def test_quant_delayed_argument_errors(lib):
+    f = lib.fp8_quant_act_delayed
+    ok = (FAKE, 4, 256, 256, FAKE, 16, FAKE, FAKE, None)
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return _rc(f, *a)
+    assert with_(2, 200) == _lib.FP8FG_ERR_ARG          # K % 128
+    assert with_(5, 0) == _lib.FP8FG_ERR_ARG            # H
+    assert with_(5, 1025) == _lib.FP8FG_ERR_ARG
+    assert with_(4, None) == _lib.FP8FG_ERR_ARG         # history
+    assert with_(4, FAKE + 4) == _lib.FP8FG_ERR_ARG     # misaligned history
+    assert with_(6, None) == _lib.FP8FG_ERR_ARG         # null q
+
+
 def test_quant_w_argument_errors(lib):
     f = lib.fp8_quant_w_128x128
     assert _rc(f, FAKE, 100, 128, 128, FAKE, FAKE, None) == _lib.FP8FG_ERR_ARG
