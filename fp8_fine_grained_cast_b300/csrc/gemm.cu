@@ -72,8 +72,11 @@ struct WarpLayout {
   static constexpr uint32_t kRegsControl = 40;
   static constexpr uint32_t kRegsPromo = 232;
   static_assert(4 * 32 * kRegsControl + kPromoWarps * 32 * kRegsPromo <= kThreads * kLaunchRegs, "register split");
-  static constexpr uint32_t kTmemBuf = BN;  // column stride of the two chunk accumulators
-  static constexpr uint32_t kTmemCols = 2 * kTmemBuf;
+  // chunk accumulators in TMEM (512 columns): two of 256 columns or four of 128, so that
+  // the MMA can run up to kNumAcc - 1 chunks ahead of the promotion warps
+  static constexpr uint32_t kNumAcc = 512 / BN;
+  static constexpr uint32_t kTmemBuf = BN;  // column stride of the chunk accumulators
+  static constexpr uint32_t kTmemCols = kNumAcc * kTmemBuf;
 };
 
 template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
@@ -91,9 +94,9 @@ struct GemmCfg : WarpLayout<BN> {
   static constexpr int kOffStaging = kOffB + STAGES * kStageB;
   static constexpr int kOffRing = kOffStaging + L::kPromoWarps * kStagingPerWarp;
   static constexpr int kOffBar = kOffRing + kSlots * kSlotFloats * 4;
-  // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], scale_full[kSlots],
-  // scale_empty[kSlots], drain
-  static constexpr int kNumBars = 2 * STAGES + 4 + 2 * kSlots + 1;
+  // full[STAGES], empty[STAGES], tmem_full[kNumAcc], tmem_empty[kNumAcc],
+  // scale_full[kSlots], scale_empty[kSlots], drain
+  static constexpr int kNumBars = 2 * STAGES + 2 * L::kNumAcc + 2 * kSlots + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffsets = kOffMisc + 16;
   static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
@@ -210,9 +213,10 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
+  constexpr uint32_t kNumAcc = Cfg::kNumAcc;
   uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint64_t* sfull = bars + 2 * STAGES + 4;
+  uint64_t* tempty = tfull + kNumAcc;
+  uint64_t* sfull = tempty + kNumAcc;
   uint64_t* sempty = sfull + kSlots;
   uint64_t* drain = sempty + kSlots;
   float* ring = reinterpret_cast<float*>(smem + Cfg::kOffRing);
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (uint32_t i = 0; i < kNumAcc; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], kPromoWarps);
     }
@@ -330,9 +334,9 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
           for (int kb = 0; kb < KB; ++kb) {
             const uint32_t st = it % STAGES;
-            const uint32_t buf = it & 1u;
+            const uint32_t buf = it % kNumAcc;
             if (!mbar_wait(&full[st], (it / STAGES) & 1u, abort_flag) ||
-                !mbar_wait(&tempty[buf], ((it >> 1) & 1u) ^ 1u, abort_flag)) {
+                !mbar_wait(&tempty[buf], ((it / kNumAcc) & 1u) ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t slot = it % kSlots;
-          const uint32_t buf = it & 1u;
+          const uint32_t buf = it % kNumAcc;
           if (!mbar_wait(&sfull[slot], (it / kSlots) & 1u, abort_flag)) {
             ok = false;
             break;
@@ -415,7 +419,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
             const uint32_t dep = __reduce_or_sync(0xFFFFFFFFu, __float_as_uint(sc));
             if (lane == 0) mbar_arrive_after(&sempty[slot], dep);
           }
-          if (!mbar_wait(&tfull[buf], (it >> 1) & 1u, abort_flag)) {
+          if (!mbar_wait(&tfull[buf], (it / kNumAcc) & 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -594,9 +598,9 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
                                      int64_t K, cudaStream_t stream, int sm_count) {
-  // 128 x 256 tiles throughout: 128-column tiles, tried for the weight-gradient shape
-  // whose 256-column tiles leave a nearly empty last wave, measured slower (the fixed
-  // per-chunk cost of the promotion handshake is paid twice as often).
+  // 128 x 256 tiles throughout: 128-column tiles (with two or with four TMEM
+  // accumulators), tried for the weight-gradient shape whose 256-column tiles leave a
+  // nearly empty last wave, measured slower on every workload.
   if (sb_kind == 0) {
     if (c_kind == 1) return run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
     if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
