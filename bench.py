@@ -328,6 +328,7 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     iters, warm = max(5, min(args.steps, 20)), 3
     out = {}
+    gemm_ws = ops.gemm_workspace(dev)
 
     xq = inputs.quant_only(dev)
     nb = xq.numel() * 3 + xq.numel() // 128 * 4
@@ -378,11 +379,17 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
     qdy, sdy = ops.quant_act_1x128(wg.dy, transposed=True)
     qxt, sxt = ops.quant_act_1x128(wg.x, transposed=True)
     fl = 2.0 * 2048 * 7168 * 4096
-    t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qxt, sxt, ops.SB_ROW_1x128, torch.float32), stream, iters, warm,
-              flush)
+    cw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
+    t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qxt, sxt, ops.SB_ROW_1x128, torch.float32, c=cw), stream, iters,
+              warm, flush)
+    t_sk = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qxt, sxt, ops.SB_ROW_1x128, torch.float32, c=cw,
+                                              workspace=gemm_ws), stream, iters, warm, flush)
     out["blockscaled_gemm wgrad 2048x7168x4096 f32"] = {"bound": "tensor", "ms": round(t, 4),
                                                         "TFLOPs": round(fl / t / 1e9, 1),
-                                                        "frac": round(fl / t / 1e9 / fp8_peak, 4)}
+                                                        "frac": round(fl / t / 1e9 / fp8_peak, 4),
+                                                        "stream_k": {"ms": round(t_sk, 4),
+                                                                     "TFLOPs": round(fl / t_sk / 1e9, 1),
+                                                                     "frac": round(fl / t_sk / 1e9 / fp8_peak, 4)}}
     del wg, qdy, sdy, qxt, sxt
 
     # the dense projection with its output kept in FP8 (codes + 1x128 scales)
@@ -423,9 +430,14 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
     fl = 2.0 * 4096 * 7168 * 18432
     t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qwt, swt, ops.SB_BLOCK_128x128, torch.bfloat16, c=dx), stream,
               iters, warm, flush)
+    t_sk = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qwt, swt, ops.SB_BLOCK_128x128, torch.bfloat16, c=dx,
+                                              workspace=gemm_ws), stream, iters, warm, flush)
     out["blockscaled_gemm dgrad 4096x7168x18432 bf16"] = {"bound": "tensor", "ms": round(t, 4),
                                                           "TFLOPs": round(fl / t / 1e9, 1),
-                                                          "frac": round(fl / t / 1e9 / fp8_peak, 4)}
+                                                          "frac": round(fl / t / 1e9 / fp8_peak, 4),
+                                                          "stream_k": {"ms": round(t_sk, 4),
+                                                                       "TFLOPs": round(fl / t_sk / 1e9, 1),
+                                                                       "frac": round(fl / t_sk / 1e9 / fp8_peak, 4)}}
     del qdy, sdy, qwt, swt, dx
 
     m = inputs.moe(dev)

@@ -43,6 +43,8 @@ SIGNATURES = {
     "fp8_quant_act_1x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_quant_w_128x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_blockscaled_gemm": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P]),
+    "fp8_blockscaled_gemm_ws": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _I64, _P]),
+    "fp8_blockscaled_gemm_workspace_bytes": (_I64, []),
     "fp8_blockscaled_gemm_e4m3": (_I, [_P, _P, _P, _P, _I, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _P, _I, _I64, _I64, _P]),
     "fp8fg_last_error": (ctypes.c_char_p, []),
@@ -113,6 +115,18 @@ def fp8_quant_w_128x128_dual(w, N, K, ldw, q, s, qt, st, stream):
 
 def fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):
     return _check(lib().fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream))
+
+
+def fp8_blockscaled_gemm_ws(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace, workspace_bytes, stream):
+    return _check(lib().fp8_blockscaled_gemm_ws(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace,
+                                                workspace_bytes, stream))
+
+
+def fp8_blockscaled_gemm_workspace_bytes():
+    n = lib().fp8_blockscaled_gemm_workspace_bytes()
+    if n < 0:
+        raise Fp8fgError(int(n), fp8fg_last_error())
+    return n
 
 
 def fp8_blockscaled_gemm_e4m3(qa, sa, qb, sb, sb_kind, c_q, c_s, M, N, K, stream):

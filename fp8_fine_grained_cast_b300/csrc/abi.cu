@@ -65,6 +65,41 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 }  // namespace
 
+namespace {
+
+// Validation and launch shared by fp8_blockscaled_gemm and fp8_blockscaled_gemm_ws.
+int gemm_checked(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind, void* c,
+                 int c_dtype, int64_t M, int64_t N, int64_t K, void* workspace, fp8fg_stream_t stream,
+                 const char* name) {
+  if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "%s: negative size", name);
+  if (sb_kind != FP8FG_SB_BLOCK_128x128 && sb_kind != FP8FG_SB_ROW_1x128) return fail(FP8FG_ERR_ARG, "%s: unknown sb_kind %d", name, sb_kind);
+  if (c_dtype != FP8FG_OUT_F32 && c_dtype != FP8FG_OUT_BF16) return fail(FP8FG_ERR_ARG, "%s: unknown c_dtype %d", name, c_dtype);
+  if (K % 128 || N % 128) return fail(FP8FG_ERR_ARG, "%s: K=%lld and N=%lld must be multiples of 128", name, (long long)K, (long long)N);
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "%s: dimension too large", name);
+  if (M == 0 || N == 0) return FP8FG_OK;
+  if (!c) return fail(FP8FG_ERR_ARG, "%s: null output pointer", name);
+  if (!aligned16(c)) return fail(FP8FG_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+  const size_t esize = c_dtype == FP8FG_OUT_BF16 ? 2 : 4;
+  if (K == 0) {
+    DeviceInfo dev;
+    if (int rc = current_device(&dev)) return rc;
+    cudaError_t err = cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * esize, reinterpret_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? FP8FG_OK : cuda_fail(err, "cudaMemsetAsync");
+  }
+  if (!qa || !sa || !qb || !sb) return fail(FP8FG_ERR_ARG, "%s: null pointer", name);
+  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb)) return fail(FP8FG_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, nullptr,
+                                                         c_dtype == FP8FG_OUT_BF16 ? 1 : 0, M, N, K,
+                                                         reinterpret_cast<cudaStream_t>(stream), dev.sm_count,
+                                                         workspace);
+  if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
+  return FP8FG_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fp8fg_last_error(void) { return g_last_error; }
@@ -183,30 +218,30 @@ int fp8_quant_w_128x128_dual(const uint16_t* w, int64_t N, int64_t K, int64_t ld
 int fp8_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,
                          void* c, int c_dtype, int64_t M, int64_t N, int64_t K, fp8fg_stream_t stream) {
   g_last_error[0] = '\0';
-  if (M < 0 || N < 0 || K < 0) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: negative size");
-  if (sb_kind != FP8FG_SB_BLOCK_128x128 && sb_kind != FP8FG_SB_ROW_1x128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: unknown sb_kind %d", sb_kind);
-  if (c_dtype != FP8FG_OUT_F32 && c_dtype != FP8FG_OUT_BF16) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: unknown c_dtype %d", c_dtype);
-  if (K % 128 || N % 128) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: K=%lld and N=%lld must be multiples of 128", (long long)K, (long long)N);
-  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: dimension too large");
-  if (M == 0 || N == 0) return FP8FG_OK;
-  if (!c) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: null output pointer");
-  if (!aligned16(c)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: pointers must be 16-byte aligned");
-  const size_t esize = c_dtype == FP8FG_OUT_BF16 ? 2 : 4;
-  if (K == 0) {
-    DeviceInfo dev;
-    if (int rc = current_device(&dev)) return rc;
-    cudaError_t err = cudaMemsetAsync(c, 0, static_cast<size_t>(M) * N * esize, reinterpret_cast<cudaStream_t>(stream));
-    return err == cudaSuccess ? FP8FG_OK : cuda_fail(err, "cudaMemsetAsync");
-  }
-  if (!qa || !sa || !qb || !sb) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: null pointer");
-  if (!aligned16(qa) || !aligned16(sa) || !aligned16(qb) || !aligned16(sb)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm: pointers must be 16-byte aligned");
+  return gemm_checked(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, nullptr, stream, "fp8_blockscaled_gemm");
+}
+
+int64_t fp8_blockscaled_gemm_workspace_bytes(void) {
+  g_last_error[0] = '\0';
   DeviceInfo dev;
   if (int rc = current_device(&dev)) return rc;
-  fp8fg::LaunchResult r = fp8fg::launch_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, nullptr,
-                                                         c_dtype == FP8FG_OUT_BF16 ? 1 : 0, M, N, K,
-                                                         reinterpret_cast<cudaStream_t>(stream), dev.sm_count);
-  if (r.err != cudaSuccess) return cuda_fail(r.err, r.what);
-  return FP8FG_OK;
+  return static_cast<int64_t>(fp8fg::gemm_workspace_bytes(dev.sm_count));
+}
+
+int fp8_blockscaled_gemm_ws(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,
+                            void* c, int c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
+                            int64_t workspace_bytes, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  if (!workspace) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_ws: null workspace");
+  if (!aligned16(workspace)) return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_ws: workspace must be 16-byte aligned");
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  const int64_t need = static_cast<int64_t>(fp8fg::gemm_workspace_bytes(dev.sm_count));
+  if (workspace_bytes < need) {
+    return fail(FP8FG_ERR_ARG, "fp8_blockscaled_gemm_ws: workspace of %lld bytes, %lld needed", (long long)workspace_bytes,
+                (long long)need);
+  }
+  return gemm_checked(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace, stream, "fp8_blockscaled_gemm_ws");
 }
 
 int fp8_blockscaled_gemm_e4m3(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,

@@ -88,6 +88,7 @@ struct GemmCfg : WarpLayout<BN> {
   // (1x128 scales of B) or one per promotion warpgroup (128x128 scales of B; a
   // warpgroup's columns lie in a single 128-column block)
   static constexpr int kSlots = (BN == 256 && SB_KIND == 0 && STAGES >= 4) ? 4 : 8;  // 4: shared memory is full
+  static constexpr int kGroup = kSlots / 2;  // chunks per scale-loader group (two groups in flight)
   static constexpr int kSbPerSlot = SB_KIND == 1 ? BN : 4;
   static constexpr int kSlotFloats = kBM + kSbPerSlot;
   static constexpr int kOffB = STAGES * kStageA;
@@ -95,8 +96,8 @@ struct GemmCfg : WarpLayout<BN> {
   static constexpr int kOffRing = kOffStaging + L::kPromoWarps * kStagingPerWarp;
   static constexpr int kOffBar = kOffRing + kSlots * kSlotFloats * 4;
   // full[STAGES], empty[STAGES], tmem_full[kNumAcc], tmem_empty[kNumAcc],
-  // scale_full[kSlots], scale_empty[kSlots], drain
-  static constexpr int kNumBars = 2 * STAGES + 2 * L::kNumAcc + 2 * kSlots + 1;
+  // scale_full[kSlots], scale_empty[kSlots], drain, head_written, tail_read
+  static constexpr int kNumBars = 2 * STAGES + 2 * L::kNumAcc + 2 * kSlots + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffOffsets = kOffMisc + 16;
   static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
@@ -140,20 +141,100 @@ struct Vec<4> {
   }
 };
 
+// Work schedule of a launch. Data-parallel: CTA c takes tiles c, c + G, ... (G = grid
+// size). Stream-K (sk_tiles > 0): the first dp_tiles tiles (a multiple of G) go data-
+// parallel, and the chunks of the last sk_tiles tiles (G <= sk_tiles < 2G) are divided
+// into G contiguous ranges of whole loader groups (grp chunks), one per CTA, in (tile,
+// chunk) order. A range is at least one tile long, so a tile is cut at most once: the
+// CTA whose range ends inside it computes its head and leaves the FP32 partial sums in
+// workspace slot c with a release flag; the next CTA, whose range starts there, computes
+// the tail last, starting its accumulators from that partial. The chunk order of every
+// element is unchanged, so the result is bit-identical to the data-parallel schedule.
+struct Schedule {
+  int dp_tiles;       // tiles scheduled data-parallel (all of them when sk_tiles == 0)
+  int sk_tiles;       // tiles in the stream-K region, 0 for none
+  int grp;            // chunks per loader group; range boundaries are multiples of it
+  int64_t sk_groups;  // sk_tiles * KB / grp
+};
+
+enum UnitKind { kWhole = 0, kHead = 1, kTail = 2 };
+
+struct Unit {
+  int tile, kb0, kb1, kind;
+};
+
+// The units of CTA c, in processing order: its head piece (so that the partial is ready
+// early), whole stream-K tiles, data-parallel tiles, its tail piece (last, so that the
+// previous CTA's partial has long been written).
+struct WorkList {
+  int n_head, n_whole, n_dp, n_tail;
+  int head_tile, head_kb1, whole0, tail_tile, tail_kb0, dp_first, stride, KB;
+  __device__ WorkList(const Schedule& s, int num_tiles, int KB_, int c, int G) {
+    KB = KB_;
+    stride = G;
+    dp_first = c;
+    if (s.sk_tiles == 0) {
+      n_head = n_whole = n_tail = 0;
+      head_tile = head_kb1 = whole0 = tail_tile = tail_kb0 = 0;
+      n_dp = c < num_tiles ? (num_tiles - 1 - c) / G + 1 : 0;
+      return;
+    }
+    const int64_t g0 = (static_cast<int64_t>(c) * s.sk_groups) / G * s.grp;
+    const int64_t g1 = (static_cast<int64_t>(c + 1) * s.sk_groups) / G * s.grp;
+    n_tail = (g0 % KB) != 0;
+    tail_tile = s.dp_tiles + static_cast<int>(g0 / KB);
+    tail_kb0 = static_cast<int>(g0 % KB);
+    n_head = (g1 % KB) != 0;
+    head_tile = s.dp_tiles + static_cast<int>(g1 / KB);
+    head_kb1 = static_cast<int>(g1 % KB);
+    whole0 = s.dp_tiles + static_cast<int>((g0 + KB - 1) / KB);
+    n_whole = s.dp_tiles + static_cast<int>(g1 / KB) - whole0;
+    n_dp = s.dp_tiles / G;
+  }
+  __device__ int count() const { return n_head + n_whole + n_dp + n_tail; }
+  __device__ Unit get(int u) const {
+    if (u < n_head) return {head_tile, 0, head_kb1, kHead};
+    u -= n_head;
+    if (u < n_whole) return {whole0 + u, 0, KB, kWhole};
+    u -= n_whole;
+    if (u < n_dp) return {dp_first + u * stride, 0, KB, kWhole};
+    return {tail_tile, tail_kb0, KB, kTail};
+  }
+};
+
+// Bounded wait for a flag another CTA sets with release semantics; the same limit and
+// abort protocol as the mbarrier waits.
+__device__ __forceinline__ bool flag_wait(const int* flag, volatile int* abort_flag) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_status(kStatusTimeout);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // Scale-loader loop of loader warp `li` (0 or 1): groups of G chunks, alternate groups
-// per warp; slot of chunk c is c % kSlots (kSlots >= 2 G). Requires KB % G == 0 so that
-// a group never straddles two tiles.
+// per warp; slot of chunk c is c % kSlots (kSlots >= 2 G). Requires KB % G == 0 and unit
+// boundaries at multiples of G, so that a group never straddles two units.
 template <int G, typename Cfg, bool GROUPED, int SB_KIND, typename Coords>
 __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M, int N, int num_tiles,
-                                                 const Coords& tile_coords, const float* __restrict__ sa,
-                                                 const float* __restrict__ sb, float* ring, uint64_t* sfull,
-                                                 uint64_t* sempty, volatile int* abort_flag) {
+                                                 const Coords& tile_coords, const WorkList& wl,
+                                                 const float* __restrict__ sa, const float* __restrict__ sb,
+                                                 float* ring, uint64_t* sfull, uint64_t* sempty,
+                                                 volatile int* abort_flag) {
   constexpr int kSlots = Cfg::kSlots;
   constexpr int BN = Cfg::kStageB / kBK;
   uint32_t it = 0;
-  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+  for (int u = 0; u < wl.count(); ++u) {
+    const Unit w = wl.get(u);
     int m_blk, n_blk, e;
-    tile_coords(t, m_blk, n_blk, e);
+    tile_coords(w.tile, m_blk, n_blk, e);
     const int m0 = m_blk * kBM;
     const int n0 = n_blk * BN;
     const int64_t step32 = static_cast<int64_t>(32) * KB;  // 32 rows of a scale matrix
@@ -161,7 +242,7 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
     const float* sb_col =
         SB_KIND == 1 ? sb + static_cast<int64_t>(n0 + lane) * KB
                      : sb + (static_cast<int64_t>(GROUPED ? e * (N / kBM) : 0) + (n0 + lane * Cfg::kCols) / kBM) * KB;
-    for (int kb0 = 0; kb0 < KB; kb0 += G, it += G) {
+    for (int kb0 = w.kb0; kb0 < w.kb1; kb0 += G, it += G) {
       if (static_cast<int>((it / G) & 1u) != li) continue;
       for (int g = 0; g < G; ++g) {
         const uint32_t c = it + g;
@@ -202,11 +283,12 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             void* __restrict__ c_out, float* __restrict__ c_scale, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
-                            int K, int num_m_tiles, int num_n_tiles) {
+                            int K, int num_m_tiles, int num_n_tiles, Schedule sched, float* __restrict__ ws_partial,
+                            int* __restrict__ ws_flags) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
   constexpr int kPromoWarps = Cfg::kPromoWarps;
-  constexpr int kGroup = kSlots / 2;   // chunks per scale-loader group (two groups in flight)
+  constexpr int kGroup = Cfg::kGroup;
   // The dynamic shared window starts 1024-byte aligned (checked below); the swizzled
   // TMA tiles and the UMMA descriptors rely on it.
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,6 +301,8 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   uint64_t* sfull = tempty + kNumAcc;
   uint64_t* sempty = sfull + kSlots;
   uint64_t* drain = sempty + kSlots;
+  uint64_t* head_written = drain + 1;  // stream-K: the promotion threads' partial sums are stored
+  uint64_t* tail_read = drain + 2;     // stream-K: the promotion threads have read the previous partial
   float* ring = reinterpret_cast<float*>(smem + Cfg::kOffRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
@@ -229,6 +313,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int KB = K / kBK;
   const int num_tiles = num_m_tiles * num_n_tiles;
+  const WorkList wl(sched, num_tiles, KB, blockIdx.x, gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -244,6 +329,8 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       mbar_init(&sempty[i], SB_KIND == 0 ? kPromoWarps : kPromoWarps * 32);
     }
     mbar_init(drain, 1);
+    mbar_init(head_written, kPromoWarps * 32);
+    mbar_init(tail_read, kPromoWarps * 32);
     *abort_flag = 0;
     *bad_args = (smem_u32(smem) & 1023u) != 0;
     fence_barrier_init();
@@ -302,12 +389,13 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         tma_prefetch_map(&tmB);
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int u = 0; ok && u < wl.count(); ++u) {
+          const Unit w = wl.get(u);
           int m_blk, n_blk, e;
-          tile_coords(t, m_blk, n_blk, e);
+          tile_coords(w.tile, m_blk, n_blk, e);
           const int a_row = m_blk * kBM;
           const int b_row = (GROUPED ? e * N : 0) + n_blk * BN;
-          for (int kb = 0; kb < KB; ++kb) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t st = it % STAGES;
             if (!mbar_wait(&empty[st], ((it / STAGES) & 1u) ^ 1u, abort_flag)) {
               ok = false;
@@ -331,8 +419,9 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-          for (int kb = 0; kb < KB; ++kb) {
+        for (int u = 0; ok && u < wl.count(); ++u) {
+          const Unit w = wl.get(u);
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t st = it % STAGES;
             const uint32_t buf = it % kNumAcc;
             if (!mbar_wait(&full[st], (it / STAGES) & 1u, abort_flag) ||
@@ -368,10 +457,10 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       // consume a third.
       const int li = warp - 2;
       if (KB % kGroup == 0) {
-        load_scales_impl<kGroup, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, sa, sb, ring,
+        load_scales_impl<kGroup, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, wl, sa, sb, ring,
                                                         sfull, sempty, abort_flag);
       } else {
-        load_scales_impl<1, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, sa, sb, ring, sfull,
+        load_scales_impl<1, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, wl, sa, sb, ring, sfull,
                                                    sempty, abort_flag);
       }
     }
@@ -388,19 +477,44 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int u = 0; ok && u < wl.count(); ++u) {
+        const Unit w = wl.get(u);
         int m_blk, n_blk, e;
-        tile_coords(t, m_blk, n_blk, e);
+        tile_coords(w.tile, m_blk, n_blk, e);
         const int m0 = m_blk * kBM;
         const int col0 = n_blk * BN + g * kCols;
 
-        // FP32 accumulators of this thread's row, in pairs for the packed FMAs
+        // FP32 accumulators of this thread's row, in pairs for the packed FMAs: zero, or
+        // for the tail of a cut tile the head's partial sums (left by the previous CTA)
         float2 acc2[kCols / 2];
-#pragma unroll
-        for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         float* acc = reinterpret_cast<float*>(acc2);
+        if (w.kind == kTail) {
+          // every promotion thread reads its row's part of the previous CTA's partial sums
+          // (once that CTA's release flag is seen); one thread then clears the flag for the
+          // next launch, after all have read. Each CTA has at most one tail unit, so the
+          // barrier completes at most once (phase 0).
+          ok = flag_wait(ws_flags + blockIdx.x - 1, abort_flag);
+          if (ok) {
+            const float4* src = reinterpret_cast<const float4*>(
+                ws_partial + (static_cast<size_t>(blockIdx.x - 1) * kBM + row) * BN + g * kCols);
+#pragma unroll
+            for (int i = 0; i < kCols / 4; ++i) {
+              const float4 v = __ldcg(src + i);
+              acc2[2 * i] = make_float2(v.x, v.y);
+              acc2[2 * i + 1] = make_float2(v.z, v.w);
+            }
+          }
+          mbar_arrive(tail_read);
+          if (threadIdx.x == kFirstPromoWarp * 32 && ok && mbar_wait(tail_read, 0, abort_flag)) {
+            ws_flags[blockIdx.x - 1] = 0;
+          }
+          if (!ok) break;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
+        }
 
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           const uint32_t slot = it % kSlots;
           const uint32_t buf = it % kNumAcc;
           if (!mbar_wait(&sfull[slot], (it / kSlots) & 1u, abort_flag)) {
@@ -485,6 +599,27 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
           }
           ++it;
         }
+        if (w.kind == kHead) {
+          // the head of a cut tile: leave the partial sums in slot blockIdx.x; once every
+          // promotion thread has stored its part (at most one head unit per CTA: phase 0),
+          // one thread releases them to the CTA that computes the tail. A thread that has
+          // given up still arrives, so the waiter never waits for it; no flag is set then.
+          if (ok) {
+            float4* dst = reinterpret_cast<float4*>(ws_partial + (static_cast<size_t>(blockIdx.x) * kBM + row) * BN +
+                                                    g * kCols);
+#pragma unroll
+            for (int i = 0; i < kCols / 4; ++i) {
+              __stcg(dst + i, make_float4(acc2[2 * i].x, acc2[2 * i].y, acc2[2 * i + 1].x, acc2[2 * i + 1].y));
+            }
+            __threadfence();
+          }
+          mbar_arrive(head_written);
+          if (threadIdx.x == kFirstPromoWarp * 32 && ok && mbar_wait(head_written, 0, abort_flag) && !*abort_flag) {
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ws_flags + blockIdx.x), "r"(1) : "memory");
+          }
+          if (!ok) break;
+          continue;
+        }
         if (!ok) break;
 
         // ------------------------------------------------------ epilogue
@@ -560,10 +695,14 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
+// Stream-K workspace: one FP32 partial tile (128 x 256) per CTA, then one flag per CTA.
+constexpr size_t kPartialTileBytes = static_cast<size_t>(kBM) * 256 * 4;
+size_t gemm_partial_bytes(int ctas) { return static_cast<size_t>(ctas) * kPartialTileBytes; }
+
 template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
 LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                       const int32_t* offsets, int E, int64_t M, int64_t N, int64_t K, int64_t b_rows, void* c,
-                      float* c_scale, cudaStream_t stream, int sm_count) {
+                      float* c_scale, cudaStream_t stream, int sm_count, void* workspace = nullptr) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   auto kernel = blockscaled_gemm_kernel<BN, STAGES, SB_KIND, OUT, GROUPED>;
   const size_t smem = Cfg::smem_bytes(E);
@@ -586,8 +725,23 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   const int num_n = static_cast<int>((N + BN - 1) / BN);
   const int64_t tiles = static_cast<int64_t>(num_m) * num_n;
   const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+  Schedule sched{static_cast<int>(tiles), 0, 1, 0};
+  float* ws_partial = nullptr;
+  int* ws_flags = nullptr;
+  const int KB = static_cast<int>(K / kBK);
+  if (workspace && tiles > grid && tiles % grid != 0) {
+    // stream-K over the last one to two waves' worth of tiles (see Schedule)
+    const int grp = KB % Cfg::kGroup == 0 ? Cfg::kGroup : 1;
+    sched.dp_tiles = static_cast<int>((tiles / grid - 1) * grid);
+    sched.sk_tiles = static_cast<int>(tiles) - sched.dp_tiles;
+    sched.grp = grp;
+    sched.sk_groups = static_cast<int64_t>(sched.sk_tiles) * KB / grp;
+    ws_partial = static_cast<float*>(workspace);
+    ws_flags = reinterpret_cast<int*>(static_cast<char*>(workspace) + gemm_partial_bytes(sm_count));
+  }
   kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, c_scale, sa, sb, offsets, E, static_cast<int>(M),
-                                           static_cast<int>(N), static_cast<int>(K), num_m, num_n);
+                                           static_cast<int>(N), static_cast<int>(K), num_m, num_n, sched,
+                                           ws_partial, ws_flags);
   err = cudaGetLastError();
   if (err != cudaSuccess) return {err, "kernel launch"};
   return {cudaSuccess, nullptr};
@@ -595,20 +749,24 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 
 }  // namespace
 
+size_t gemm_workspace_bytes(int sm_count) {
+  return (gemm_partial_bytes(sm_count) + static_cast<size_t>(sm_count) * sizeof(int) + 255) / 256 * 256;
+}
+
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
-                                     int64_t K, cudaStream_t stream, int sm_count) {
+                                     int64_t K, cudaStream_t stream, int sm_count, void* workspace) {
   // 128 x 256 tiles throughout: 128-column tiles (with two or with four TMEM
   // accumulators), tried for the weight-gradient shape whose 256-column tiles leave a
   // nearly empty last wave, measured slower on every workload.
   if (sb_kind == 0) {
-    if (c_kind == 1) return run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
-    if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
-    return run_gemm<256, 4, 0, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+    if (c_kind == 1) return run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
+    if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count, workspace);
+    return run_gemm<256, 4, 0, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
   }
-  if (c_kind == 1) return run_gemm<256, 3, 1, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
-  if (c_kind == 2) return run_gemm<256, 3, 1, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
-  return run_gemm<256, 3, 1, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+  if (c_kind == 1) return run_gemm<256, 3, 1, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
+  if (c_kind == 2) return run_gemm<256, 3, 1, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count, workspace);
+  return run_gemm<256, 3, 1, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
 }
 
 LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,

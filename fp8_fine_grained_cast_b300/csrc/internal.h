@@ -45,9 +45,12 @@ struct LaunchResult {
 };
 
 // c_kind: 0 FP32 C, 1 BF16 C, 2 E4M3 codes of C with 1x128 scales c_scale[M][N/128].
+// workspace: null for the data-parallel schedule, else at least gemm_workspace_bytes(sm_count)
+// bytes (zero-initialized before first use) for the stream-K schedule.
 LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
-                                     int64_t K, cudaStream_t stream, int sm_count);
+                                     int64_t K, cudaStream_t stream, int sm_count, void* workspace = nullptr);
+size_t gemm_workspace_bytes(int sm_count);
 
 LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                  const int32_t* offsets, int E, int64_t Mtot, void* c, int c_bf16, int64_t N,

@@ -123,8 +123,17 @@ def quant_w_128x128_dual(w: torch.Tensor, out=None):
     return q, s, qt, st
 
 
-def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out_dtype=torch.bfloat16, c=None):
-    """C = A . B^T from E4M3 codes and scales; C [M, N] in bf16 or float32."""
+def gemm_workspace(device) -> torch.Tensor:
+    """A zero-filled workspace for the stream-K GEMM on `device` (reusable across calls)."""
+    with torch.cuda.device(device):
+        n = _lib.fp8_blockscaled_gemm_workspace_bytes()
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out_dtype=torch.bfloat16, c=None,
+                     workspace=None):
+    """C = A . B^T from E4M3 codes and scales; C [M, N] in bf16 or float32. With a
+    workspace (see gemm_workspace) the stream-K schedule runs; the result is the same."""
     for t, n, dt, nd in ((qa, "qa", torch.uint8, 2), (sa, "sa", torch.float32, 2), (qb, "qb", torch.uint8, 2),
                          (sb, "sb", torch.float32, 2)):
         _need(t, dt, n, nd)
@@ -138,8 +147,14 @@ def blockscaled_gemm(qa, sa, qb, sb, sb_kind: int = SB_BLOCK_128x128, out_dtype=
     if out_dtype not in (torch.bfloat16, torch.float32):
         raise TypeError("out_dtype must be torch.bfloat16 or torch.float32")
     c = torch.empty((M, N), dtype=out_dtype, device=qa.device) if c is None else c
-    _lib.fp8_blockscaled_gemm(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), sb_kind, c.data_ptr(),
-                              c_dtype, M, N, K, _stream())
+    if workspace is None:
+        _lib.fp8_blockscaled_gemm(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), sb_kind, c.data_ptr(),
+                                  c_dtype, M, N, K, _stream())
+    else:
+        _need(workspace, torch.uint8, "workspace", 1)
+        _lib.fp8_blockscaled_gemm_ws(qa.data_ptr(), sa.data_ptr(), qb.data_ptr(), sb.data_ptr(), sb_kind,
+                                     c.data_ptr(), c_dtype, M, N, K, workspace.data_ptr(), workspace.numel(),
+                                     _stream())
     return c
 
 

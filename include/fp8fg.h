@@ -166,6 +166,29 @@ int fp8_blockscaled_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, 
                          fp8fg_stream_t stream);
 
 /*
+ * The same GEMM as fp8_blockscaled_gemm, scheduled stream-K with a caller-owned
+ * workspace (no counterpart on the pages: a scheduling choice for this GPU). When the
+ * tiles do not fill whole waves of CTAs, the chunks of the last one to two waves' worth
+ * of tiles are divided evenly over the CTAs; a tile cut between two CTAs has its head's
+ * FP32 partial sums passed through the workspace, and the tail continues from them in the
+ * same chunk order, so C is bit-identical to fp8_blockscaled_gemm.
+ *
+ * workspace: DEVICE memory of at least fp8_blockscaled_gemm_workspace_bytes() bytes,
+ *     16-byte aligned, zero-filled before its first use. The library leaves it ready for
+ *     the next call; after a call that reported FP8FG_ERR_TIMEOUT, zero it again. Calls
+ *     that share a workspace must not run concurrently (order them on one stream).
+ * Other arguments, layouts and errors as fp8_blockscaled_gemm; FP8FG_ERR_ARG for a null,
+ * misaligned or too small workspace.
+ */
+int fp8_blockscaled_gemm_ws(const uint8_t *qa, const float *sa, const uint8_t *qb, const float *sb, int sb_kind,
+                            void *c, int c_dtype, int64_t M, int64_t N, int64_t K, void *workspace,
+                            int64_t workspace_bytes, fp8fg_stream_t stream);
+
+/* Workspace size for fp8_blockscaled_gemm_ws on the current device (about 128 KB per SM);
+ * a negative error code if the device is unsupported. */
+int64_t fp8_blockscaled_gemm_workspace_bytes(void);
+
+/*
  * Block-scaled FP8 GEMM whose output is quantized to E4M3 in 1x128 tiles (activations
  * kept in FP8 between layers: "Unified E4M3 format in DeepSeek-V3", memory section; the
  * quantization is the one of fp8_quant_act_1x128).

@@ -155,6 +155,18 @@ def test_gemm_e4m3_argument_errors(lib):
     assert with_(7, 0) == _lib.FP8FG_OK                 # empty
 
 
+def test_gemm_ws_argument_errors(lib):
+    f = lib.fp8_blockscaled_gemm_ws
+    ok = [FAKE, FAKE, FAKE, FAKE, 0, FAKE, 1, 128, 256, 256, FAKE, 1 << 30, None]
+
+    def with_(i, v):
+        a = list(ok)
+        a[i] = v
+        return _rc(f, *a)
+    assert with_(10, None) == _lib.FP8FG_ERR_ARG        # null workspace
+    assert with_(10, FAKE + 8) == _lib.FP8FG_ERR_ARG    # misaligned workspace
+
+
 def test_grouped_argument_errors(lib):
     f = lib.fp8_grouped_gemm
     ok = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 512, FAKE, 1, 256, 256, None]
