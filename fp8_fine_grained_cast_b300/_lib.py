@@ -45,6 +45,7 @@ SIGNATURES = {
     "fp8_blockscaled_gemm": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P]),
     "fp8_blockscaled_gemm_ws": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _I64, _P]),
     "fp8_blockscaled_gemm_workspace_bytes": (_I64, []),
+    "fp8_blockscaled_gemm_sk_static": (_I, [_P, _P, _P, _P, _I, _P, _I, _I64, _I64, _I64, _P]),
     "fp8_blockscaled_gemm_e4m3": (_I, [_P, _P, _P, _P, _I, _P, _P, _I64, _I64, _I64, _P]),
     "fp8_grouped_gemm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _P, _I, _I64, _I64, _P]),
     "fp8fg_last_error": (ctypes.c_char_p, []),
@@ -120,6 +121,10 @@ def fp8_blockscaled_gemm(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):
 def fp8_blockscaled_gemm_ws(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace, workspace_bytes, stream):
     return _check(lib().fp8_blockscaled_gemm_ws(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace,
                                                 workspace_bytes, stream))
+
+
+def fp8_blockscaled_gemm_sk_static(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream):
+    return _check(lib().fp8_blockscaled_gemm_sk_static(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, stream))
 
 
 def fp8_blockscaled_gemm_workspace_bytes():

@@ -30,6 +30,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int supported = 0;
   int known = 0;
+  void* scratch = nullptr;  // static stream-K workspace, set up on first use
 };
 
 constexpr int kMaxDevices = 64;
@@ -62,6 +63,34 @@ int current_device(DeviceInfo* out) {
 }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Address of the current device's static stream-K workspace, found once per device;
+// the first call also clears its flags (which must start at zero) with a synchronous
+// memset, so it must not happen inside stream capture.
+int static_scratch(void** out) {
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
+  DeviceInfo info;
+  if (int rc = current_device(&info)) return rc;
+  std::lock_guard<std::mutex> lock(g_devices_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (!d.scratch) {
+    void* p = nullptr;
+    size_t bytes = 0;
+    if ((err = fp8fg::gemm_static_scratch(&p, &bytes)) != cudaSuccess) return cuda_fail(err, "cudaGetSymbolAddress");
+    if (fp8fg::gemm_workspace_bytes(d.sm_count) > bytes) {
+      return fail(FP8FG_ERR_UNSUPPORTED, "static GEMM workspace holds %zu bytes, %zu needed for %d SMs", bytes,
+                  fp8fg::gemm_workspace_bytes(d.sm_count), d.sm_count);
+    }
+    if ((err = cudaMemset(p, 0, bytes)) != cudaSuccess) return cuda_fail(err, "cudaMemset");
+    d.scratch = p;
+  }
+  *out = d.scratch;
+  return FP8FG_OK;
+}
+
+
 
 }  // namespace
 
@@ -242,6 +271,15 @@ int fp8_blockscaled_gemm_ws(const uint8_t* qa, const float* sa, const uint8_t* q
                 (long long)need);
   }
   return gemm_checked(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, workspace, stream, "fp8_blockscaled_gemm_ws");
+}
+
+int fp8_blockscaled_gemm_sk_static(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
+                                   int sb_kind, void* c, int c_dtype, int64_t M, int64_t N, int64_t K,
+                                   fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  void* scratch = nullptr;
+  if (int rc = static_scratch(&scratch)) return rc;
+  return gemm_checked(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, scratch, stream, "fp8_blockscaled_gemm_sk_static");
 }
 
 int fp8_blockscaled_gemm_e4m3(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb, int sb_kind,

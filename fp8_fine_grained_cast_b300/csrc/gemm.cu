@@ -749,6 +749,19 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 
 }  // namespace
 
+// Library-owned stream-K workspace for fp8_blockscaled_gemm_sk_static: room for the
+// partial tiles and flags of a device with up to kStaticScratchSms SMs (about 20 MB). One
+// copy per device; calls that use it must not overlap.
+constexpr int kStaticScratchSms = 160;
+constexpr size_t kStaticScratchBytes =
+    (static_cast<size_t>(kStaticScratchSms) * (kPartialTileBytes + sizeof(int)) + 255) / 256 * 256;
+static __device__ __align__(256) uint8_t g_gemm_scratch[kStaticScratchBytes];
+
+cudaError_t gemm_static_scratch(void** ptr, size_t* bytes) {
+  *bytes = kStaticScratchBytes;
+  return cudaGetSymbolAddress(ptr, g_gemm_scratch);
+}
+
 size_t gemm_workspace_bytes(int sm_count) {
   return (gemm_partial_bytes(sm_count) + static_cast<size_t>(sm_count) * sizeof(int) + 255) / 256 * 256;
 }

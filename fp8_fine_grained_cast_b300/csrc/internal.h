@@ -51,6 +51,8 @@ LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const u
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
                                      int64_t K, cudaStream_t stream, int sm_count, void* workspace = nullptr);
 size_t gemm_workspace_bytes(int sm_count);
+// Address (current device) and size of the library-owned static stream-K workspace.
+cudaError_t gemm_static_scratch(void** ptr, size_t* bytes);
 
 LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                                  const int32_t* offsets, int E, int64_t Mtot, void* c, int c_bf16, int64_t N,

@@ -184,6 +184,22 @@ int fp8_blockscaled_gemm_ws(const uint8_t *qa, const float *sa, const uint8_t *q
                             void *c, int c_dtype, int64_t M, int64_t N, int64_t K, void *workspace,
                             int64_t workspace_bytes, fp8fg_stream_t stream);
 
+/*
+ * fp8_blockscaled_gemm_ws with a library-owned workspace: the call allocates nothing
+ * (no counterpart on the pages; it makes the stream-K schedule available to callers that
+ * cannot hand over device memory). The workspace is one file-scope static device array
+ * per device, sized for devices with up to 160 SMs (about 20 MB; FP8FG_ERR_UNSUPPORTED
+ * beyond that). Its address is looked up, and its flags cleared with a synchronous
+ * memset, on the first call on each device, so make that first call before capturing a
+ * stream into a graph. Every call on a device uses the same array: calls that overlap in
+ * time (on different streams, or from different threads without ordering) race on it and
+ * give undefined results; order them on one stream. Arguments, results (bit-identical to
+ * fp8_blockscaled_gemm) and errors otherwise as fp8_blockscaled_gemm.
+ */
+int fp8_blockscaled_gemm_sk_static(const uint8_t *qa, const float *sa, const uint8_t *qb, const float *sb,
+                                   int sb_kind, void *c, int c_dtype, int64_t M, int64_t N, int64_t K,
+                                   fp8fg_stream_t stream);
+
 /* Workspace size for fp8_blockscaled_gemm_ws on the current device (about 128 KB per SM);
  * a negative error code if the device is unsupported. */
 int64_t fp8_blockscaled_gemm_workspace_bytes(void);
