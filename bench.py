@@ -55,7 +55,7 @@ def load_peaks():
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm.cu", "quant.cu", "common.cuh"):
+    for f in ("gemm.cu", "quant.cu", "common.cuh", "e4m3.cuh"):
         h.update(open(os.path.join(ROOT, "fp8_fine_grained_cast_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -99,7 +99,8 @@ struct GemmCfg : WarpLayout<BN> {
   // scale_full[kSlots], scale_empty[kSlots], drain, head_written, tail_read
   static constexpr int kNumBars = 2 * STAGES + 2 * L::kNumAcc + 2 * kSlots + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffOffsets = kOffMisc + 16;
+  static constexpr int kOffWork = kOffMisc + 16;  // WorkDesc of this CTA
+  static constexpr int kOffOffsets = kOffWork + 48;
   static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
   // epilogue box: 32 rows x 128 bytes of FP32 (OUT 0), BF16 (OUT 1) or E4M3 codes (OUT 2)
   static constexpr int kBoxCols = OUT == 0 ? 32 : OUT == 1 ? 64 : 128;
@@ -163,44 +164,47 @@ struct Unit {
   int tile, kb0, kb1, kind;
 };
 
-// The units of CTA c, in processing order: its head piece (so that the partial is ready
-// early), whole stream-K tiles, data-parallel tiles, its tail piece (last, so that the
-// previous CTA's partial has long been written).
-struct WorkList {
-  int n_head, n_whole, n_dp, n_tail;
-  int head_tile, head_kb1, whole0, tail_tile, tail_kb0, dp_first, stride, KB;
-  __device__ WorkList(const Schedule& s, int num_tiles, int KB_, int c, int G) {
-    KB = KB_;
-    stride = G;
-    dp_first = c;
-    if (s.sk_tiles == 0) {
-      n_head = n_whole = n_tail = 0;
-      head_tile = head_kb1 = whole0 = tail_tile = tail_kb0 = 0;
-      n_dp = c < num_tiles ? (num_tiles - 1 - c) / G + 1 : 0;
-      return;
-    }
+// The units of this CTA (c = blockIdx.x of G = gridDim.x), in processing order: its head
+// piece (so that the partial is ready early), whole stream-K tiles, data-parallel
+// tiles, its tail piece (last, so that the previous CTA's partial has long been
+// written). One thread derives the description once into shared memory; the roles read
+// it there, so that none keeps it (or the 64-bit arithmetic behind it) in registers.
+struct WorkDesc {
+  int n_units, n_head, head_tile, head_kb1, n_whole, whole0, n_dp, tail_tile, tail_kb0;
+};
+
+__device__ __forceinline__ void work_desc_init(const Schedule& s, int num_tiles, int KB, WorkDesc* wd) {
+  const int c = blockIdx.x, G = gridDim.x;
+  WorkDesc d{};
+  if (s.sk_tiles == 0) {
+    d.n_dp = c < num_tiles ? (num_tiles - 1 - c) / G + 1 : 0;
+  } else {
     const int64_t g0 = (static_cast<int64_t>(c) * s.sk_groups) / G * s.grp;
     const int64_t g1 = (static_cast<int64_t>(c + 1) * s.sk_groups) / G * s.grp;
-    n_tail = (g0 % KB) != 0;
-    tail_tile = s.dp_tiles + static_cast<int>(g0 / KB);
-    tail_kb0 = static_cast<int>(g0 % KB);
-    n_head = (g1 % KB) != 0;
-    head_tile = s.dp_tiles + static_cast<int>(g1 / KB);
-    head_kb1 = static_cast<int>(g1 % KB);
-    whole0 = s.dp_tiles + static_cast<int>((g0 + KB - 1) / KB);
-    n_whole = s.dp_tiles + static_cast<int>(g1 / KB) - whole0;
-    n_dp = s.dp_tiles / G;
+    d.n_head = (g1 % KB) != 0;
+    d.head_tile = s.dp_tiles + static_cast<int>(g1 / KB);
+    d.head_kb1 = static_cast<int>(g1 % KB);
+    d.whole0 = s.dp_tiles + static_cast<int>((g0 + KB - 1) / KB);
+    d.n_whole = s.dp_tiles + static_cast<int>(g1 / KB) - d.whole0;
+    d.n_dp = s.dp_tiles / G;
+    d.tail_tile = s.dp_tiles + static_cast<int>(g0 / KB);
+    d.tail_kb0 = static_cast<int>(g0 % KB);
+    d.n_units = (g0 % KB) != 0;  // the tail, counted below
   }
-  __device__ int count() const { return n_head + n_whole + n_dp + n_tail; }
-  __device__ Unit get(int u) const {
-    if (u < n_head) return {head_tile, 0, head_kb1, kHead};
-    u -= n_head;
-    if (u < n_whole) return {whole0 + u, 0, KB, kWhole};
-    u -= n_whole;
-    if (u < n_dp) return {dp_first + u * stride, 0, KB, kWhole};
-    return {tail_tile, tail_kb0, KB, kTail};
-  }
-};
+  d.n_units += d.n_head + d.n_whole + d.n_dp;
+  *wd = d;
+}
+
+template <bool SK>
+__device__ __forceinline__ Unit unit_get(const WorkDesc* wd, int KB, int u) {
+  if constexpr (!SK) return {static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x), 0, KB, kWhole};
+  if (u < wd->n_head) return {wd->head_tile, 0, wd->head_kb1, kHead};
+  u -= wd->n_head;
+  if (u < wd->n_whole) return {wd->whole0 + u, 0, KB, kWhole};
+  u -= wd->n_whole;
+  if (u < wd->n_dp) return {static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x), 0, KB, kWhole};
+  return {wd->tail_tile, wd->tail_kb0, KB, kTail};
+}
 
 // Bounded wait for a flag another CTA sets with release semantics; the same limit and
 // abort protocol as the mbarrier waits.
@@ -222,17 +226,18 @@ __device__ __forceinline__ bool flag_wait(const int* flag, volatile int* abort_f
 // Scale-loader loop of loader warp `li` (0 or 1): groups of G chunks, alternate groups
 // per warp; slot of chunk c is c % kSlots (kSlots >= 2 G). Requires KB % G == 0 and unit
 // boundaries at multiples of G, so that a group never straddles two units.
-template <int G, typename Cfg, bool GROUPED, int SB_KIND, typename Coords>
+template <int G, typename Cfg, bool GROUPED, int SB_KIND, bool SK, typename Coords>
 __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M, int N, int num_tiles,
-                                                 const Coords& tile_coords, const WorkList& wl,
+                                                 const Coords& tile_coords, const WorkDesc* wd,
                                                  const float* __restrict__ sa, const float* __restrict__ sb,
                                                  float* ring, uint64_t* sfull, uint64_t* sempty,
                                                  volatile int* abort_flag) {
   constexpr int kSlots = Cfg::kSlots;
   constexpr int BN = Cfg::kStageB / kBK;
   uint32_t it = 0;
-  for (int u = 0; u < wl.count(); ++u) {
-    const Unit w = wl.get(u);
+  const int n_units = wd->n_units;
+  for (int u = 0; u < n_units; ++u) {
+    const Unit w = unit_get<SK>(wd, KB, u);
     int m_blk, n_blk, e;
     tile_coords(w.tile, m_blk, n_blk, e);
     const int m0 = m_blk * kBM;
@@ -278,12 +283,13 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
   }
 }
 
-template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
+template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED, bool SK>
 __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             void* __restrict__ c_out, float* __restrict__ c_scale, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
-                            int K, int num_m_tiles, int num_n_tiles, Schedule sched, float* __restrict__ ws_partial,
+                            int K, int num_m_tiles, int num_n_tiles, const __grid_constant__ Schedule sched,
+                            float* __restrict__ ws_partial,
                             int* __restrict__ ws_flags) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
@@ -308,12 +314,12 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* bad_args = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + Cfg::kOffOffsets);
+  WorkDesc* wd = reinterpret_cast<WorkDesc*>(smem + Cfg::kOffWork);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KB = K / kBK;
   const int num_tiles = num_m_tiles * num_n_tiles;
-  const WorkList wl(sched, num_tiles, KB, blockIdx.x, gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -331,6 +337,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(head_written, kPromoWarps * 32);
     mbar_init(tail_read, kPromoWarps * 32);
+    work_desc_init(sched, num_tiles, KB, wd);
     *abort_flag = 0;
     *bad_args = (smem_u32(smem) & 1023u) != 0;
     fence_barrier_init();
@@ -389,8 +396,8 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         tma_prefetch_map(&tmB);
         uint32_t it = 0;
         bool ok = true;
-        for (int u = 0; ok && u < wl.count(); ++u) {
-          const Unit w = wl.get(u);
+        for (int u = 0; ok && u < wd->n_units; ++u) {
+          const Unit w = unit_get<SK>(wd, KB, u);
           int m_blk, n_blk, e;
           tile_coords(w.tile, m_blk, n_blk, e);
           const int a_row = m_blk * kBM;
@@ -419,8 +426,8 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
         uint32_t it = 0;
         bool ok = true;
-        for (int u = 0; ok && u < wl.count(); ++u) {
-          const Unit w = wl.get(u);
+        for (int u = 0; ok && u < wd->n_units; ++u) {
+          const Unit w = unit_get<SK>(wd, KB, u);
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t st = it % STAGES;
             const uint32_t buf = it % kNumAcc;
@@ -457,10 +464,10 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       // consume a third.
       const int li = warp - 2;
       if (KB % kGroup == 0) {
-        load_scales_impl<kGroup, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, wl, sa, sb, ring,
+        load_scales_impl<kGroup, Cfg, GROUPED, SB_KIND, SK>(li, lane, KB, M, N, num_tiles, tile_coords, wd, sa, sb, ring,
                                                         sfull, sempty, abort_flag);
       } else {
-        load_scales_impl<1, Cfg, GROUPED, SB_KIND>(li, lane, KB, M, N, num_tiles, tile_coords, wl, sa, sb, ring, sfull,
+        load_scales_impl<1, Cfg, GROUPED, SB_KIND, SK>(li, lane, KB, M, N, num_tiles, tile_coords, wd, sa, sb, ring, sfull,
                                                    sempty, abort_flag);
       }
     }
@@ -477,22 +484,26 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = 0; ok && u < wl.count(); ++u) {
-        const Unit w = wl.get(u);
+      for (int u = 0; ok && u < wd->n_units; ++u) {
+        const Unit w = unit_get<SK>(wd, KB, u);
         int m_blk, n_blk, e;
         tile_coords(w.tile, m_blk, n_blk, e);
         const int m0 = m_blk * kBM;
         const int col0 = n_blk * BN + g * kCols;
 
-        // FP32 accumulators of this thread's row, in pairs for the packed FMAs: zero, or
+        // FP32 accumulators of this thread's row, in pairs for the packed FMAs: zero, plus
         // for the tail of a cut tile the head's partial sums (left by the previous CTA)
         float2 acc2[kCols / 2];
         float* acc = reinterpret_cast<float*>(acc2);
+#pragma unroll
+        for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         if (w.kind == kTail) {
-          // every promotion thread reads its row's part of the previous CTA's partial sums
-          // (once that CTA's release flag is seen); one thread then clears the flag for the
+          // every promotion thread adds its row's part of the previous CTA's partial sums
+          // (once that CTA's release flag is seen) to its zeroed accumulators: exact, since
+          // sums that start from +0 are never -0; one thread then clears the flag for the
           // next launch, after all have read. Each CTA has at most one tail unit, so the
-          // barrier completes at most once (phase 0).
+          // barrier completes at most once (phase 0). (Loading the partial into the
+          // accumulators directly made the compiler spill them.)
           ok = flag_wait(ws_flags + blockIdx.x - 1, abort_flag);
           if (ok) {
             const float4* src = reinterpret_cast<const float4*>(
@@ -500,8 +511,10 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kCols / 4; ++i) {
               const float4 v = __ldcg(src + i);
-              acc2[2 * i] = make_float2(v.x, v.y);
-              acc2[2 * i + 1] = make_float2(v.z, v.w);
+              acc2[2 * i].x += v.x;
+              acc2[2 * i].y += v.y;
+              acc2[2 * i + 1].x += v.z;
+              acc2[2 * i + 1].y += v.w;
             }
           }
           mbar_arrive(tail_read);
@@ -509,9 +522,6 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
             ws_flags[blockIdx.x - 1] = 0;
           }
           if (!ok) break;
-        } else {
-#pragma unroll
-          for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         }
 
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
@@ -699,12 +709,12 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 constexpr size_t kPartialTileBytes = static_cast<size_t>(kBM) * 256 * 4;
 size_t gemm_partial_bytes(int ctas) { return static_cast<size_t>(ctas) * kPartialTileBytes; }
 
-template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED>
+template <int BN, int STAGES, int SB_KIND, int OUT, bool GROUPED, bool SK = false>
 LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
                       const int32_t* offsets, int E, int64_t M, int64_t N, int64_t K, int64_t b_rows, void* c,
                       float* c_scale, cudaStream_t stream, int sm_count, void* workspace = nullptr) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
-  auto kernel = blockscaled_gemm_kernel<BN, STAGES, SB_KIND, OUT, GROUPED>;
+  auto kernel = blockscaled_gemm_kernel<BN, STAGES, SB_KIND, OUT, GROUPED, SK>;
   const size_t smem = Cfg::smem_bytes(E);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return {err, "cudaFuncSetAttribute(max dynamic shared memory)"};
@@ -729,7 +739,7 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   float* ws_partial = nullptr;
   int* ws_flags = nullptr;
   const int KB = static_cast<int>(K / kBK);
-  if (workspace && tiles > grid && tiles % grid != 0) {
+  if (SK && workspace && tiles > grid && tiles % grid != 0) {
     // stream-K over the last one to two waves' worth of tiles (see Schedule)
     const int grp = KB % Cfg::kGroup == 0 ? Cfg::kGroup : 1;
     sched.dp_tiles = static_cast<int>((tiles / grid - 1) * grid);
@@ -771,15 +781,26 @@ LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const u
                                      int64_t K, cudaStream_t stream, int sm_count, void* workspace) {
   // 128 x 256 tiles throughout: 128-column tiles (with two or with four TMEM
   // accumulators), tried for the weight-gradient shape whose 256-column tiles leave a
-  // nearly empty last wave, measured slower on every workload.
+  // nearly empty last wave, measured slower on every workload. The stream-K variants
+  // (with a workspace) are separate instantiations, so that the data-parallel kernel
+  // carries none of their code.
+  const bool sk = workspace != nullptr;
   if (sb_kind == 0) {
-    if (c_kind == 1) return run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
-    if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count, workspace);
-    return run_gemm<256, 4, 0, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
+    if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
+    if (c_kind == 1) {
+      return sk ? run_gemm<256, 4, 0, 1, false, true>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace)
+                : run_gemm<256, 4, 0, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+    }
+    return sk ? run_gemm<256, 4, 0, 0, false, true>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace)
+              : run_gemm<256, 4, 0, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
   }
-  if (c_kind == 1) return run_gemm<256, 3, 1, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
-  if (c_kind == 2) return run_gemm<256, 3, 1, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count, workspace);
-  return run_gemm<256, 3, 1, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace);
+  if (c_kind == 2) return run_gemm<256, 3, 1, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);
+  if (c_kind == 1) {
+    return sk ? run_gemm<256, 3, 1, 1, false, true>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace)
+              : run_gemm<256, 3, 1, 1, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
+  }
+  return sk ? run_gemm<256, 3, 1, 0, false, true>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count, workspace)
+            : run_gemm<256, 3, 1, 0, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, nullptr, stream, sm_count);
 }
 
 LaunchResult launch_grouped_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, const float* sb,
