@@ -327,6 +327,14 @@ def run_ours(args, rank, world, local):
     return line
 
 
+def flush_l2(flush):
+    """Evict L2 before a timed launch: write a buffer larger than L2 (512 MB), then read
+    half of it, so that the write-back of the flush's own dirty lines happens here and
+    not inside the timed kernel (ncu's cache-controlled durations agree with this)."""
+    flush.zero_()
+    flush[: flush.numel() // 2].max()
+
+
 def timed(fn, stream, iters, warm, flush):
     """Mean device time (ms) of fn over `iters` runs, L2 flushed before each run."""
     import torch
@@ -334,7 +342,7 @@ def timed(fn, stream, iters, warm, flush):
         fn()
     ts = []
     for _ in range(iters):
-        flush.zero_()
+        flush_l2(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
