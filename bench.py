@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -53,10 +54,17 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank space, so that the hash follows the code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "".join(text.split())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in ("gemm.cu", "quant.cu", "common.cuh", "e4m3.cuh"):
-        h.update(open(os.path.join(ROOT, "fp8_fine_grained_cast_b300", "csrc", f), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, "fp8_fine_grained_cast_b300", "csrc", f)).read()).encode())
     return h.hexdigest()[:16]
 
 

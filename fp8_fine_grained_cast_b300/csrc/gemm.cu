@@ -14,9 +14,9 @@
 //              one of two TMEM accumulators (BN columns each), the first with the
 //              accumulate flag cleared, so that each accumulator holds exactly one
 //              chunk's partial sum P[m][n] = sum_{k in chunk} qa[m][k] qb[n][k].
-//   warp 2     scale loader: per chunk, the 128 row scales of A and the column (or
-//              column-block) scales of B into a shared-memory ring
-//   warp 3     idle (it completes the first warpgroup, which gives its registers up)
+//   warps 2-3  scale loaders: per chunk, the 128 row scales of A and the column (or
+//              column-block) scales of B into a shared-memory ring, alternate groups of
+//              chunks per warp
 //   warps 4-11 promotion and epilogue: two warpgroups; warpgroup g owns columns
 //              [g BN/2, (g+1) BN/2) of the tile and warp (w % 4) owns TMEM lanes (rows)
 //              32 (w % 4) .. +31. Per chunk: tcgen05.ld the partial sums, release the
@@ -25,7 +25,11 @@
 //              compute chunk kb+1 into the other accumulator. After the last chunk the
 //              accumulators are rounded to the output type, transposed through a small
 //              swizzled shared-memory buffer per warp and written with coalesced 16-byte
-//              stores (the TMA unit stays free for the operand loads).
+//              stores (the TMA unit stays free for the operand loads). The output can
+//              also be E4M3 codes with 1x128 scales: each promotion thread holds exactly
+//              one 1x128 tile of C.
+// Schedules: data-parallel (CTA c takes tiles c, c + G, ...) or, with a workspace,
+// stream-K for a partial last wave (see Schedule below), as separate instantiations.
 // Every mbarrier wait is bounded (about one second); a wait that runs out raises a
 // CTA-wide abort flag and records a timeout in the device status word, every role
 // leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
