@@ -172,3 +172,17 @@ def test_gpu_call_rejects_bad_shape(cuda_device):
     with pytest.raises(_lib.Fp8fgError) as ei:
         ops.quant_act_1x128(x)
     assert ei.value.code == _lib.FP8FG_ERR_ARG
+
+
+def test_transposed_many_blocks_and_ragged_columns(cuda_device):
+    """The persistent transposed quantizer with about two, and more than two, blocks per
+    CTA, and with a ragged last column block over many row blocks, against the oracle."""
+    sm = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    rng = np.random.default_rng(33)
+    for mb, K in ((4 * sm // 8, 1024), (4 * sm // 8 + 1, 1024), (300, 264)):
+        x = rng.standard_normal((128 * mb, K)).astype(np.float32)
+        x[rng.random(x.shape) < 0.001] *= 40.0
+        x[5:133, 3] = 0.0                                                 # one all-zero tile
+        xd = bf16_dev(x, cuda_device)
+        q, s = ops.quant_act_1x128(xd, transposed=True)
+        assert_same_quant(q, s, *O.quant_act_1x128_transposed(f32(xd)))
