@@ -105,7 +105,7 @@ struct GemmCfg : WarpLayout<BN> {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffWork = kOffMisc + 16;  // WorkDesc of this CTA
   static constexpr int kOffOffsets = kOffWork + 48;
-  static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (E + 1) : 0); }
+  static size_t smem_bytes(int E) { return kOffOffsets + (GROUPED ? 4 * (3 * E + 2) : 0); }
   // epilogue box: 32 rows x 128 bytes of FP32 (OUT 0), BF16 (OUT 1) or E4M3 codes (OUT 2)
   static constexpr int kBoxCols = OUT == 0 ? 32 : OUT == 1 ? 64 : 128;
   static_assert(OUT != 2 || L::kCols == 128, "an E4M3 output row slice is one 1x128 tile");
@@ -367,23 +367,54 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     }
     __syncthreads();
   }
+  // grouped: row tiles in an order that alternates between the largest and the smallest
+  // experts (s_sorted: experts by size, descending, by an O(E^2) rank count for E <= 512,
+  // else in index order; s_cum: their row-tile prefix sums)
+  int32_t* s_sorted = s_off + E + 1;
+  int32_t* s_cum = s_sorted + E;
+  if constexpr (GROUPED) {
+    if (E <= 512) {
+      for (int i = threadIdx.x; i < E; i += blockDim.x) {
+        const int si = s_off[i + 1] - s_off[i];
+        int rank = 0;
+        for (int j = 0; j < E; ++j) {
+          const int sj = s_off[j + 1] - s_off[j];
+          rank += (sj > si) || (sj == si && j < i);
+        }
+        s_sorted[rank] = i;
+      }
+    } else {
+      for (int i = threadIdx.x; i < E; i += blockDim.x) s_sorted[i] = i;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_cum[0] = 0;
+      for (int q = 0; q < E; ++q) s_cum[q + 1] = s_cum[q] + (s_off[s_sorted[q] + 1] - s_off[s_sorted[q]]) / kBM;
+    }
+    __syncthreads();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const bool run = !*bad_args;
 
   // tile t -> (m block, n block, expert). Dense: m fastest, so that the CTAs working at
   // the same time share B tiles (and A, which fits in L2). Grouped: n fastest, so that
-  // consecutive tiles share an expert's rows and concurrent tiles share its weights.
+  // consecutive tiles share an expert's rows and concurrent tiles share its weights; the
+  // row tiles themselves alternate between the largest and the smallest experts, so that
+  // weight streaming (small experts) and tensor work (large experts reusing their weights
+  // from L2) overlap across the SMs instead of coming in separate phases.
   auto tile_coords = [&](int t, int& m_blk, int& n_blk, int& e) {
     if constexpr (GROUPED) {
       n_blk = t % num_n_tiles;
-      m_blk = t / num_n_tiles;
-      const int m0 = m_blk * kBM;
+      const int pos = t / num_n_tiles;
+      // alternate: even positions from the front of the size-sorted row tiles, odd from the back
+      const int a = (pos & 1) ? num_m_tiles - 1 - (pos >> 1) : (pos >> 1);
       int lo = 0, hi = E - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (s_off[mid] <= m0) lo = mid; else hi = mid - 1;
+        if (s_cum[mid] <= a) lo = mid; else hi = mid - 1;
       }
-      e = lo;
+      e = s_sorted[lo];
+      m_blk = s_off[e] / kBM + (a - s_cum[lo]);
     } else {
       m_blk = t % num_m_tiles;
       n_blk = t / num_m_tiles;
