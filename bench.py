@@ -385,10 +385,9 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
     hist[:16] = amax0
     nb = xq.numel() * 3 + xq.numel() // 128 * 4
 
-    def delayed_step():
-        ops.quant_act_delayed(xq, hist)
-        hist[:16] = amax0                        # keep the recorded maxima fixed between runs
-    t = timed(delayed_step, stream, iters, warm, flush)
+    # every run quantizes the same tensor, whose max |x| equals the recorded maxima, so the
+    # history's maximum (hence the scale) stays the same from run to run without a reset
+    t = timed(lambda: ops.quant_act_delayed(xq, hist), stream, iters, warm, flush)
     x2 = (xq.float() * 1.5).to(torch.bfloat16)
     qd, sd = ops.quant_act_delayed(x2, hist)
     qo, so = ops.quant_act_1x128(x2)
