@@ -370,6 +370,20 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
     out = {}
     gemm_ws = ops.gemm_workspace(dev)
 
+    # The fixed cost of one launch under this protocol (L2 flushed, two events): each
+    # quantizer on a single 128 x 128 tile. It bounds the fraction that the small
+    # tensors below can reach, whatever the streaming rate.
+    x1 = inputs.gaussian_bf16((128, 128), 1.0, dev, 0, 99)
+    floor = {"events_only": timed(lambda: None, stream, iters, warm, flush),
+             "quant_act_1x128": timed(lambda: ops.quant_act_1x128(x1), stream, iters, warm, flush),
+             "quant_act_1x128 transposed": timed(lambda: ops.quant_act_1x128(x1, transposed=True), stream, iters,
+                                                 warm, flush),
+             "quant_act_1x128_dual": timed(lambda: ops.quant_act_1x128_dual(x1), stream, iters, warm, flush),
+             "quant_w_128x128": timed(lambda: ops.quant_w_128x128(x1), stream, iters, warm, flush)}
+    out["launch floor: one 128x128 tile per call"] = {k: round(v * 1e3, 2) for k, v in floor.items()}
+    out["launch floor: one 128x128 tile per call"]["unit"] = "us"
+    del x1
+
     xq = inputs.quant_only(dev)
     nb = xq.numel() * 3 + xq.numel() // 128 * 4
     t = timed(lambda: ops.quant_act_1x128(xq), stream, iters, warm, flush)
