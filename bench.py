@@ -369,15 +369,17 @@ def timed(fn, stream, iters, warm, flush):
     return statistics.mean(ts)
 
 
-def plain_fp8_gemm_check(dev, secs=1.5):
+def plain_fp8_gemm_check(dev, m=M, n=N, k=K, secs=1.5, flush=None):
     """Measured confirmation of the FP8 denominator: the library's plain FP8 GEMM
     (cuBLASLt through torch._scaled_mm, one scale per tensor, no fine-grained scaling) on
-    the dense-projection shape, as a burst (median of single launches) and as a loop of
-    about `secs` seconds. Used only as a reference rate, outside every timed region."""
+    a GEMM shape (the dense projection by default), as a burst (median of single launches)
+    and as a loop of about `secs` seconds. Used only as a reference rate, outside every
+    timed region. With `flush`, L2 is flushed before each burst launch, as for the rows."""
     import torch
-    a = torch.randn(M, K, device=dev).to(torch.float8_e4m3fn)
-    b = torch.randn(N, K, device=dev).to(torch.float8_e4m3fn)
+    a = torch.randn(m, k, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(n, k, device=dev).to(torch.float8_e4m3fn)
     one = torch.tensor(1.0, device=dev)
+    flops = 2.0 * m * n * k
 
     def f():
         return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
@@ -386,6 +388,8 @@ def plain_fp8_gemm_check(dev, secs=1.5):
     torch.cuda.synchronize()
     ts = []
     for _ in range(10):
+        if flush is not None:
+            flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         f()
@@ -393,17 +397,17 @@ def plain_fp8_gemm_check(dev, secs=1.5):
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
     t_burst = statistics.median(ts)
-    n = max(1, int(secs / (t_burst * 1e-3)))
+    reps = max(1, int(secs / (t_burst * 1e-3)))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(n):
+    for _ in range(reps):
         f()
     e1.record()
     torch.cuda.synchronize()
-    t_loop = e0.elapsed_time(e1) / n
-    return {"kernel": f"cuBLASLt per-tensor FP8 GEMM (torch._scaled_mm) {M}x{N}x{K}, bf16 out",
-            "burst_tflops": round(GEMM_FLOPS / (t_burst * 1e-3) / 1e12, 1),
-            "sustained_tflops": round(GEMM_FLOPS / (t_loop * 1e-3) / 1e12, 1)}
+    t_loop = e0.elapsed_time(e1) / reps
+    return {"kernel": f"cuBLASLt per-tensor FP8 GEMM (torch._scaled_mm) {m}x{n}x{k}, bf16 out",
+            "burst_tflops": round(flops / (t_burst * 1e-3) / 1e12, 1),
+            "sustained_tflops": round(flops / (t_loop * 1e-3) / 1e12, 1)}
 
 
 def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
@@ -489,6 +493,9 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                                         "stream_k": {"ms": round(t_sk, 4),
                                                                      "TFLOPs": round(fl / t_sk / 1e9, 1),
                                                                      "frac": round(fl / t_sk / 1e9 / fp8_peak, 4)}}
+    ref = plain_fp8_gemm_check(dev, 2048, 7168, 4096, secs=0.2, flush=flush)
+    out["blockscaled_gemm wgrad 2048x7168x4096 f32"]["plain_fp8_same_shape"] = {
+        "kernel": ref["kernel"], "TFLOPs": ref["burst_tflops"], "ours_stream_k_over_it": round(fl / t_sk / 1e9 / ref["burst_tflops"], 4)}
     del wg, qdy, sdy, qxt, sxt
 
     # the dense projection with its output kept in FP8 (codes + 1x128 scales)
@@ -537,6 +544,9 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                                           "stream_k": {"ms": round(t_sk, 4),
                                                                        "TFLOPs": round(fl / t_sk / 1e9, 1),
                                                                        "frac": round(fl / t_sk / 1e9 / fp8_peak, 4)}}
+    ref = plain_fp8_gemm_check(dev, 4096, 7168, 18432, secs=0.2, flush=flush)
+    out["blockscaled_gemm dgrad 4096x7168x18432 bf16"]["plain_fp8_same_shape"] = {
+        "kernel": ref["kernel"], "TFLOPs": ref["burst_tflops"], "ours_stream_k_over_it": round(fl / t_sk / 1e9 / ref["burst_tflops"], 4)}
     del qdy, sdy, qwt, swt, dx
 
     m = inputs.moe(dev)
