@@ -1,0 +1,32 @@
+"""Helpers of bench.py: the kernel-source hash that ties recorded DRAM traffic to the
+code it was measured on (CPU), and the plain FP8 GEMM reference rate (GPU)."""
+import pytest
+
+import bench
+
+
+def test_source_hash_ignores_comments_and_layout():
+    code = "int f(int x) {\n  return x + 1;  // one more\n}\n"
+    same = "/* header */\nint f(int x) { return x + 1; }\n// trailing note\n"
+    other = "int f(int x) { return x + 2; }\n"
+    assert bench._code_only(code) == bench._code_only(same)
+    assert bench._code_only(code) != bench._code_only(other)
+
+
+def test_traffic_lookup_needs_the_recorded_hash(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        "# kernel hash bytes\nk_current 0123456789abcdef 1234\nk_stale 0000000000000000 99\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0123456789abcdef")
+    assert bench.profiled_traffic("k_current") == 1234
+    assert bench.profiled_traffic("k_stale") is None
+    assert bench.profiled_traffic("k_absent") is None
+
+
+@pytest.mark.gpu
+def test_plain_fp8_reference_reports_its_shape(cuda_device):
+    r = bench.plain_fp8_gemm_check(cuda_device, 256, 512, 1024, secs=0.05)
+    assert "256x512x1024" in r["kernel"]
+    assert 0.0 < r["burst_tflops"] < 20000.0
+    assert 0.0 < r["sustained_tflops"] < 20000.0
