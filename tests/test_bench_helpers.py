@@ -30,3 +30,13 @@ def test_plain_fp8_reference_reports_its_shape(cuda_device):
     assert "256x512x1024" in r["kernel"]
     assert 0.0 < r["burst_tflops"] < 20000.0
     assert 0.0 < r["sustained_tflops"] < 20000.0
+
+
+def test_rescale_touches_only_tensor_rows():
+    rows = {"g": {"bound": "tensor", "TFLOPs": 1000.0, "frac": 0.3, "stream_k": {"TFLOPs": 1500.0, "frac": 0.4}},
+            "q": {"bound": "hbm", "GBps": 5000.0, "frac": 0.8},
+            "floor": {"events_only": 1.2}}
+    bench.rescale_tensor_fracs(rows, 4000.0)
+    assert rows["g"]["frac"] == 0.25 and rows["g"]["stream_k"]["frac"] == 0.375
+    assert rows["q"]["frac"] == 0.8
+    assert rows["floor"] == {"events_only": 1.2}
