@@ -389,8 +389,9 @@ def plain_fp8_gemm_check(dev, m=M, n=N, k=K, secs=1.5, flush=None):
     (cuBLASLt through torch._scaled_mm, one scale per tensor, no fine-grained scaling) on
     a GEMM shape (the dense projection by default), as a burst (median of single launches)
     and, if `secs` > 0, as a loop of about `secs` seconds. A loop at the full tensor rate
-    leaves the part power-capped for a while, so the rows take the burst only. Used only as a reference rate, outside every
-    timed region. With `flush`, L2 is flushed before each burst launch, as for the rows."""
+    leaves the part power-capped for a while, so the rows take the burst only. Used only
+    as a reference rate, outside every timed region. With `flush`, L2 is flushed before
+    each burst launch, as for the rows."""
     import torch
     a = torch.randn(m, k, device=dev).to(torch.float8_e4m3fn)
     b = torch.randn(n, k, device=dev).to(torch.float8_e4m3fn)
