@@ -64,10 +64,14 @@ int current_device(DeviceInfo* out) {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
-// Address of the current device's static stream-K workspace, found once per device;
-// the first call also clears its flags (which must start at zero) with a synchronous
-// memset, so it must not happen inside stream capture.
-int static_scratch(void** out) {
+// Address of the current device's static stream-K workspace, found once per device
+// with cudaGetSymbolAddress (the array's host-side name is not a device address). The
+// first call on a device also zero-fills the array with an asynchronous memset on the
+// caller's stream, ordered before the GEMM launched next on that stream; make that
+// first call outside stream capture. The release flags need no further clearing: a
+// launch only accepts its own epoch (see next_streamk_epoch), and its tails clear the
+// flags they consumed.
+int static_scratch(void** out, cudaStream_t stream) {
   int dev = -1;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err, "cudaGetDevice");
@@ -83,7 +87,7 @@ int static_scratch(void** out) {
       return fail(FP8FG_ERR_UNSUPPORTED, "static GEMM workspace holds %zu bytes, %zu needed for %d SMs", bytes,
                   fp8fg::gemm_workspace_bytes(d.sm_count), d.sm_count);
     }
-    if ((err = cudaMemset(p, 0, bytes)) != cudaSuccess) return cuda_fail(err, "cudaMemset");
+    if ((err = cudaMemsetAsync(p, 0, bytes, stream)) != cudaSuccess) return cuda_fail(err, "cudaMemsetAsync");
     d.scratch = p;
   }
   *out = d.scratch;
@@ -278,7 +282,7 @@ int fp8_blockscaled_gemm_sk_static(const uint8_t* qa, const float* sa, const uin
                                    fp8fg_stream_t stream) {
   g_last_error[0] = '\0';
   void* scratch = nullptr;
-  if (int rc = static_scratch(&scratch)) return rc;
+  if (int rc = static_scratch(&scratch, reinterpret_cast<cudaStream_t>(stream))) return rc;
   return gemm_checked(qa, sa, qb, sb, sb_kind, c, c_dtype, M, N, K, scratch, stream, "fp8_blockscaled_gemm_sk_static");
 }
 

@@ -35,6 +35,8 @@
 // leaves its loop, in-flight copies and MMAs are drained (bounded) and TMEM is freed.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "e4m3.cuh"
 #include "internal.h"
@@ -210,14 +212,15 @@ __device__ __forceinline__ Unit unit_get(const WorkDesc* wd, int KB, int u) {
   return {wd->tail_tile, wd->tail_kb0, KB, kTail};
 }
 
-// Bounded wait for a flag another CTA sets with release semantics; the same limit and
-// abort protocol as the mbarrier waits.
-__device__ __forceinline__ bool flag_wait(const int* flag, volatile int* abort_flag) {
+// Bounded wait until a flag that another CTA sets with release semantics holds this
+// launch's epoch; the same limit and abort protocol as the mbarrier waits. A value left
+// by an earlier launch that gave up before its tail read it (another epoch) is ignored.
+__device__ __forceinline__ bool flag_wait(const int* flag, int epoch, volatile int* abort_flag) {
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v != 0) return true;
+    if (v == epoch) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       record_status(kStatusTimeout);
@@ -293,8 +296,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
                             void* __restrict__ c_out, float* __restrict__ c_scale, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
                             int K, int num_m_tiles, int num_n_tiles, const __grid_constant__ Schedule sched,
-                            float* __restrict__ ws_partial,
-                            int* __restrict__ ws_flags) {
+                            float* __restrict__ ws_partial, int* __restrict__ ws_flags, int sk_epoch) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
   constexpr int kPromoWarps = Cfg::kPromoWarps;
@@ -534,12 +536,12 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         for (int i = 0; i < kCols / 2; ++i) acc2[i] = make_float2(0.0f, 0.0f);
         if (w.kind == kTail) {
           // every promotion thread adds its row's part of the previous CTA's partial sums
-          // (once that CTA's release flag is seen) to its zeroed accumulators: exact, since
-          // sums that start from +0 are never -0; one thread then clears the flag for the
-          // next launch, after all have read. Each CTA has at most one tail unit, so the
-          // barrier completes at most once (phase 0). (Loading the partial into the
-          // accumulators directly made the compiler spill them.)
-          ok = flag_wait(ws_flags + blockIdx.x - 1, abort_flag);
+          // (once that CTA's release flag holds this launch's epoch) to its zeroed
+          // accumulators: exact, since sums that start from +0 are never -0; one thread
+          // then clears the flag, after all have read. Each CTA has at most one tail
+          // unit, so the barrier completes at most once (phase 0). (Loading the partial
+          // into the accumulators directly made the compiler spill them.)
+          ok = flag_wait(ws_flags + blockIdx.x - 1, sk_epoch, abort_flag);
           if (ok) {
             const float4* src = reinterpret_cast<const float4*>(
                 ws_partial + (static_cast<size_t>(blockIdx.x - 1) * kBM + row) * BN + g * kCols);
@@ -660,7 +662,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
           }
           mbar_arrive(head_written);
           if (threadIdx.x == kFirstPromoWarp * 32 && ok && mbar_wait(head_written, 0, abort_flag) && !*abort_flag) {
-            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ws_flags + blockIdx.x), "r"(1) : "memory");
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ws_flags + blockIdx.x), "r"(sk_epoch) : "memory");
           }
           if (!ok) break;
           continue;
@@ -740,6 +742,17 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
+// Epoch of a stream-K launch: a head CTA releases its partial sums by writing the epoch
+// into its flag, the tail CTA waits for exactly that value and then clears the flag.
+// Distinct launches get distinct epochs (1 .. 2^31 - 1, cycling), so a flag left set
+// by a launch whose tail gave up (a bounded wait that ran out) cannot release a later
+// launch's tail early.
+std::atomic<uint32_t> g_streamk_epoch{0};
+
+int next_streamk_epoch() {
+  return static_cast<int>(g_streamk_epoch.fetch_add(1, std::memory_order_relaxed) % 0x7FFFFFFFu) + 1;
+}
+
 // Stream-K workspace: one FP32 partial tile (128 x 256) per CTA, then one flag per CTA.
 constexpr size_t kPartialTileBytes = static_cast<size_t>(kBM) * 256 * 4;
 size_t gemm_partial_bytes(int ctas) { return static_cast<size_t>(ctas) * kPartialTileBytes; }
@@ -773,6 +786,7 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
   Schedule sched{static_cast<int>(tiles), 0, 1, 0};
   float* ws_partial = nullptr;
   int* ws_flags = nullptr;
+  int epoch = 0;
   const int KB = static_cast<int>(K / kBK);
   if (SK && workspace && tiles > grid && tiles % grid != 0) {
     // stream-K over the last one to two waves' worth of tiles (see Schedule)
@@ -783,10 +797,11 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
     sched.sk_groups = static_cast<int64_t>(sched.sk_tiles) * KB / grp;
     ws_partial = static_cast<float*>(workspace);
     ws_flags = reinterpret_cast<int*>(static_cast<char*>(workspace) + gemm_partial_bytes(sm_count));
+    epoch = next_streamk_epoch();
   }
   kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, c_scale, sa, sb, offsets, E, static_cast<int>(M),
                                            static_cast<int>(N), static_cast<int>(K), num_m, num_n, sched,
-                                           ws_partial, ws_flags);
+                                           ws_partial, ws_flags, epoch);
   err = cudaGetLastError();
   if (err != cudaSuccess) return {err, "kernel launch"};
   return {cudaSuccess, nullptr};

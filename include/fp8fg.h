@@ -175,8 +175,10 @@ int fp8_blockscaled_gemm(const uint8_t *qa, const float *sa, const uint8_t *qb, 
  *
  * workspace: DEVICE memory of at least fp8_blockscaled_gemm_workspace_bytes() bytes,
  *     16-byte aligned, zero-filled before its first use. The library leaves it ready for
- *     the next call; after a call that reported FP8FG_ERR_TIMEOUT, zero it again. Calls
- *     that share a workspace must not run concurrently (order them on one stream).
+ *     the next call, also after a call that reported FP8FG_ERR_TIMEOUT: a cut tile's
+ *     partial sums are released by a flag holding a value unique to the launch, so a
+ *     flag left set by a launch that gave up is ignored by later launches. Calls that
+ *     share a workspace must not run concurrently (order them on one stream).
  * Other arguments, layouts and errors as fp8_blockscaled_gemm; FP8FG_ERR_ARG for a null,
  * misaligned or too small workspace.
  */
@@ -189,9 +191,11 @@ int fp8_blockscaled_gemm_ws(const uint8_t *qa, const float *sa, const uint8_t *q
  * (no counterpart on the pages; it makes the stream-K schedule available to callers that
  * cannot hand over device memory). The workspace is one file-scope static device array
  * per device, sized for devices with up to 160 SMs (about 20 MB; FP8FG_ERR_UNSUPPORTED
- * beyond that). Its address is looked up, and its flags cleared with a synchronous
- * memset, on the first call on each device, so make that first call before capturing a
- * stream into a graph. Every call on a device uses the same array: calls that overlap in
+ * beyond that). Its address is looked up, and the array zero-filled by an asynchronous
+ * memset on `stream`, on the first call on each device, so make that first call before
+ * capturing a stream into a graph. Its release flags stay valid after a call that
+ * reported FP8FG_ERR_TIMEOUT (see fp8_blockscaled_gemm_ws), so the array never needs to
+ * be cleared again. Every call on a device uses the same array: calls that overlap in
  * time (on different streams, or from different threads without ordering) race on it and
  * give undefined results; order them on one stream. Arguments, results (bit-identical to
  * fp8_blockscaled_gemm) and errors otherwise as fp8_blockscaled_gemm.

@@ -10,7 +10,8 @@ tolerance is 1e-4 of max|C|); then
     at most), zero tiles exactly;
   - a code may differ only by one E4M3 step, and only where the oracle's quotient
     C / s lies within 2e-5 * 448 of the rounding midpoint between the two codes;
-  - at most 0.5 % of the codes may differ.
+  - at most 0.5 % of the codes may differ on the small random cases, and on the full
+    dense projection at most the cap below, about twice the count observed there.
 """
 import numpy as np
 import pytest
@@ -21,6 +22,10 @@ from oracle import fp8_oracle as O
 from tests.test_gpu_gemm import dev, f32, random_quantized
 
 pytestmark = pytest.mark.gpu
+
+# Codes of the full dense test (98 sampled rows x 18432 columns = 1.8M codes) that may
+# differ from the oracle by one step next to a rounding midpoint.
+DENSE_FULL_MAX_DIFFERING = 2000
 
 
 def run(qa, sa, qb, sb, sb_kind, device):
@@ -42,6 +47,7 @@ def assert_close(q, s, q_ref, s_ref, c_ref):
     assert rel.size == 0 or rel.max() <= 1e-5, rel.max()
     bad = np.argwhere(q != q_ref)
     assert len(bad) <= 0.005 * q.size, f"{len(bad)} of {q.size} codes differ"
+    print(f"e4m3-out codes differing from the oracle: {len(bad)} of {q.size}")
     if len(bad):
         m, n = bad[:, 0], bad[:, 1]
         dg = O.e4m3_decode(q[m, n])
@@ -52,6 +58,7 @@ def assert_close(q, s, q_ref, s_ref, c_ref):
         assert np.all(np.abs(ag - ar) <= 1), "codes more than one step apart"
         mid = (dg + dr) / 2.0
         assert np.all(np.abs(y - mid) <= 2e-5 * 448), np.max(np.abs(y - mid))
+    return len(bad)
 
 
 @pytest.mark.parametrize("sb_kind", [O.SB_BLOCK_128x128, O.SB_ROW_1x128])
@@ -110,7 +117,8 @@ def test_e4m3_out_dense_projection_full(cuda_device):
     rows = np.array(sorted(set(np.random.default_rng(3).choice(4096, 96, replace=False).tolist()) | {0, 4095}))
     q_ref, s_ref, c_ref = O.blockscaled_gemm_e4m3(rq, rs, wq, ws, rows=rows)
     sel = torch.from_numpy(rows).to(cuda_device)
-    assert_close(cq[sel].cpu().numpy(), cs[sel].cpu().numpy(), q_ref, s_ref, c_ref)
+    n_bad = assert_close(cq[sel].cpu().numpy(), cs[sel].cpu().numpy(), q_ref, s_ref, c_ref)
+    assert n_bad <= DENSE_FULL_MAX_DIFFERING, n_bad
 
 
 def test_e4m3_out_k_zero_and_empty(cuda_device):

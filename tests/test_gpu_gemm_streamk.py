@@ -77,3 +77,27 @@ def test_streamk_refuses_small_workspace(cuda_device):
     with pytest.raises(_lib.Fp8fgError) as ei:
         ops.blockscaled_gemm(qa, s, qa, s[:1], ops.SB_BLOCK_128x128, torch.float32, workspace=small)
     assert ei.value.code == _lib.FP8FG_ERR_ARG
+
+
+@pytest.mark.parametrize("stale", [1, -1])
+def test_streamk_ignores_flags_left_by_an_earlier_launch(cuda_device, stale):
+    """A launch whose tail gave up (a bounded wait that ran out) leaves its release flag
+    set. Planting such flags on the host (the value 1, which an earlier launch of this
+    process used as its epoch, and -1) must not change the result: a tail accepts only
+    its own launch's epoch."""
+    rng = np.random.default_rng(404)
+    M, N, K = 20480, 256, 512
+    qa, sa, qb, sb = random_quantized(rng, M, N, K, O.SB_BLOCK_128x128)
+    args = (dev(qa, cuda_device), dev(sa, cuda_device), dev(qb, cuda_device), dev(sb, cuda_device))
+    ws = ops.gemm_workspace(cuda_device)
+    c_dp = ops.blockscaled_gemm(*args, O.SB_BLOCK_128x128, torch.float32)
+    for _ in range(2):                          # this process's epochs are past 1 from here on
+        ops.blockscaled_gemm(*args, O.SB_BLOCK_128x128, torch.float32, workspace=ws)
+    ops.sync_status()
+    sm = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    flags = ws[sm * 128 * 256 * 4: sm * 128 * 256 * 4 + 4 * sm].view(torch.int32)
+    ws[: sm * 128 * 256 * 4].view(torch.float32).fill_(1.0e30)    # garbage partial sums
+    flags.fill_(stale)
+    c_sk = ops.blockscaled_gemm(*args, O.SB_BLOCK_128x128, torch.float32, workspace=ws)
+    ops.sync_status()
+    assert torch.equal(c_sk, c_dp)

@@ -88,6 +88,39 @@ def test_moe_config_full(cuda_device):
         assert np.all(f32(c[lo + counts[e]:hi]) == 0.0)
 
 
+def test_moe_config_every_expert(cuda_device):
+    """The full MoE workload, every one of the 256 experts: its first and last routed
+    rows against the oracle on one 128-column block of the output (the oracle quantizes
+    only that block's 128 weight rows, which the 128x128 blocks keep independent), and
+    every padding row of every expert exactly zero."""
+    m = inputs.moe(cuda_device)
+    E, N, K = m.w.shape
+    qa, sa = ops.quant_act_1x128(m.a)
+    qw, sw = ops.quant_w_128x128(m.w.view(E * N, K))
+    c = ops.grouped_gemm(qa, sa, qw.view(E, N, K), sw.view(E, N // 128, K // 128), m.offsets, torch.bfloat16)
+    ops.sync_status()
+    counts = np.array(m.rows_per_expert)
+    off = m.offsets_host
+    pad_rows = [np.arange(off[e] + counts[e], off[e + 1]) for e in range(E)]
+    pad_rows = torch.from_numpy(np.concatenate(pad_rows)).to(cuda_device)
+    assert pad_rows.numel() == int(off[E]) - int(counts.sum())
+    assert torch.count_nonzero(c[pad_rows]).item() == 0
+    checked = 0
+    for e in range(E):
+        if counts[e] == 0:
+            continue
+        rows = np.unique([off[e], off[e] + counts[e] - 1])
+        nb = e % (N // 128)
+        x_rows = f32(m.a[torch.from_numpy(rows).to(cuda_device)])
+        rq, rs = O.quant_act_1x128(x_rows)
+        wq, ws = O.quant_w_128x128(f32(m.w[e, 128 * nb:128 * (nb + 1)]))
+        ref = O.blockscaled_gemm(rq, rs, wq, ws)
+        got = f32(c[torch.from_numpy(rows).to(cuda_device), 128 * nb:128 * (nb + 1)])
+        assert O.relative_error(got, ref) <= 8e-3, e
+        checked += 1
+    assert checked == int((counts > 0).sum())
+
+
 def test_bad_offsets_are_reported(cuda_device):
     rng = np.random.default_rng(2)
     qa, sa, qb, sb, off = small_case(rng, [128, 128], 128, 128)

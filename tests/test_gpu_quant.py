@@ -182,7 +182,8 @@ def test_transposed_many_blocks_and_ragged_columns(cuda_device):
     for mb, K in ((4 * sm // 8, 1024), (4 * sm // 8 + 1, 1024), (300, 264)):
         x = rng.standard_normal((128 * mb, K)).astype(np.float32)
         x[rng.random(x.shape) < 0.001] *= 40.0
-        x[5:133, 3] = 0.0                                                 # one all-zero tile
+        x[128:256, 3] = 0.0                                               # an all-zero tile (tokens 128-255)
+        x[5:133, 5] = 0.0                                                 # zeros straddling two tiles
         xd = bf16_dev(x, cuda_device)
         q, s = ops.quant_act_1x128(xd, transposed=True)
         assert_same_quant(q, s, *O.quant_act_1x128_transposed(f32(xd)))

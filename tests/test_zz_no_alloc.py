@@ -60,3 +60,24 @@ def test_static_workspace_gemm_small_problem(cuda_device):
     _static(a, s1, b, s2, O.SB_BLOCK_128x128, c)
     ops.sync_status()
     assert torch.equal(c, ref)
+
+
+def test_static_workspace_after_a_recorded_timeout(cuda_device):
+    """A device-side wait that ran out (the self-test kernel) is reported once; the
+    static-workspace GEMM then still equals the data-parallel GEMM on two calls in a row."""
+    _lib.fp8fg_selftest_wait_timeout(torch.cuda.current_stream().cuda_stream)
+    with pytest.raises(_lib.Fp8fgError) as ei:
+        ops.sync_status()
+    assert ei.value.code == _lib.FP8FG_ERR_TIMEOUT
+    M, N, K = 20480, 512, 1152
+    rng = np.random.default_rng(79)
+    xa = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16).to(cuda_device)
+    xb = torch.from_numpy((rng.standard_normal((N, K)) * 0.02).astype(np.float32)).to(torch.bfloat16).to(cuda_device)
+    qa, sa = ops.quant_act_1x128(xa)
+    qb, sb = ops.quant_w_128x128(xb)
+    ref = ops.blockscaled_gemm(qa, sa, qb, sb, O.SB_BLOCK_128x128, torch.float32)
+    for _ in range(2):
+        c = torch.full((M, N), 5.0, dtype=torch.float32, device=cuda_device)
+        _static(qa, sa, qb, sb, O.SB_BLOCK_128x128, c)
+        ops.sync_status()
+        assert torch.equal(c, ref)
