@@ -64,7 +64,7 @@ def _code_only(text: str) -> str:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("gemm.cu", "quant.cu", "common.cuh", "e4m3.cuh"):
+    for f in ("gemm.cu", "gemm_sched.cuh", "quant.cu", "common.cuh", "e4m3.cuh"):
         h.update(_code_only(open(os.path.join(ROOT, "fp8_fine_grained_cast_b300", "csrc", f)).read()).encode())
     return h.hexdigest()[:16]
 
@@ -509,8 +509,14 @@ def bench_rows(dev, stream, hbm_peak, fp8_peak, args):
                                                      "GBps": round(nb / t / 1e6, 1),
                                                      "frac": round(nb / t / 1e6 / hbm_peak, 4),
                                                      "algorithmic_bytes": nb}
-    qdy, sdy = ops.quant_act_1x128(wg.dy, transposed=True)
-    qxt, sxt = ops.quant_act_1x128(wg.x, transposed=True)
+    # both operands of the weight-gradient GEMM in one launch
+    nb = sum(t_.numel() * 3 + t_.numel() // 128 * 4 for t_ in (wg.dy, wg.x))
+    o_p = ops.quant_act_1x128_transposed_pair(wg.dy, wg.x)
+    t = timed(lambda: ops.quant_act_1x128_transposed_pair(wg.dy, wg.x, out=o_p), stream, iters, warm, flush)
+    out["quant_act_1x128_transposed_pair dY [4096,2048] + X [4096,7168]"] = {
+        "bound": "hbm", "ms": round(t, 4), "GBps": round(nb / t / 1e6, 1), "frac": round(nb / t / 1e6 / hbm_peak, 4),
+        "algorithmic_bytes": nb}
+    qdy, sdy, qxt, sxt = o_p
     fl = 2.0 * 2048 * 7168 * 4096
     cw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
     t = timed(lambda: ops.blockscaled_gemm(qdy, sdy, qxt, sxt, ops.SB_ROW_1x128, torch.float32, c=cw), stream, iters,
@@ -618,6 +624,38 @@ def _host_cores():
         return os.cpu_count() or 1
 
 
+def _openblas_threads(n):
+    """Without threadpoolctl: the OpenBLAS library numpy loaded, found in this process's
+    memory map and called through its exported thread-count functions. n=None reads the
+    count; otherwise sets it to n and returns a function that restores the old count
+    (None if no OpenBLAS was found)."""
+    import ctypes
+    paths = set()
+    try:
+        for line in open("/proc/self/maps"):
+            part = line.split()[-1]
+            if "openblas" in part and ".so" in part:
+                paths.add(part)
+    except OSError:
+        return None
+    for path in sorted(paths):
+        lib = ctypes.CDLL(path)
+        for prefix in ("scipy_openblas", "openblas"):
+            for suffix in ("64_", ""):
+                get = getattr(lib, f"{prefix}_get_num_threads{suffix}", None)
+                put = getattr(lib, f"{prefix}_set_num_threads{suffix}", None)
+                if get is None or put is None:
+                    continue
+                get.restype = ctypes.c_int
+                put.argtypes = [ctypes.c_int]
+                if n is None:
+                    return int(get())
+                old = int(get())
+                put(int(n))
+                return lambda: put(old)
+    return None
+
+
 class OracleThreads:
     """Runs the oracle on every host core: BLAS (the float64 GEMM) limited to exactly
     `n` threads through threadpoolctl, and the numpy quantizers applied to row blocks
@@ -633,17 +671,24 @@ class OracleThreads:
     def __enter__(self):
         from concurrent.futures import ThreadPoolExecutor
 
-        import numpy  # noqa: F401  (loads the BLAS library, so that threadpoolctl can find and limit it)
-        from threadpoolctl import threadpool_info, threadpool_limits
-        self._limits = threadpool_limits(limits=self.n, user_api="blas")
-        info = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
-        self.blas_threads = max(info) if info else 0
+        import numpy  # noqa: F401  (loads the BLAS library, so that it can be found and limited)
+        try:
+            from threadpoolctl import threadpool_info, threadpool_limits
+        except ImportError:
+            self._restore = _openblas_threads(self.n)
+            self.blas_threads = _openblas_threads(None)
+        else:
+            limits = threadpool_limits(limits=self.n, user_api="blas")
+            self._restore = limits.restore_original_limits
+            info = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+            self.blas_threads = max(info) if info else None
         self.pool = ThreadPoolExecutor(self.n)
         return self
 
     def __exit__(self, *exc):
         self.pool.shutdown()
-        self._limits.restore_original_limits()
+        if callable(self._restore):
+            self._restore()
 
     def rows(self, fn, x, unit=128):
         """fn over row blocks of x (block boundaries on multiples of `unit` rows),
@@ -744,6 +789,7 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     case = args.case
+    ws = ops.gemm_workspace(dev) if args.sk else None     # stream-K schedule for the dense GEMMs
     if case == "qrow":
         x = inputs.quant_only(dev)
         fn = lambda: ops.quant_act_1x128(x)
@@ -752,6 +798,11 @@ def run_case(args):
         x = inputs.wgrad(dev).x
         fn = lambda: ops.quant_act_1x128(x, transposed=True)
         work = {"bytes": x.numel() * 3 + x.numel() // 128 * 4}
+    elif case == "qcolpair":
+        wg = inputs.wgrad(dev)
+        o_p = ops.quant_act_1x128_transposed_pair(wg.dy, wg.x)
+        fn = lambda: ops.quant_act_1x128_transposed_pair(wg.dy, wg.x, out=o_p)
+        work = {"bytes": sum(t_.numel() * 3 + t_.numel() // 128 * 4 for t_ in (wg.dy, wg.x))}
     elif case == "qw":
         w = inputs.dense(dev, M=128).w
         fn = lambda: ops.quant_w_128x128(w)
@@ -762,14 +813,15 @@ def run_case(args):
         qw, sw = ops.quant_w_128x128(d.w)
         del d
         c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        fn = lambda: ops.blockscaled_gemm(qx, sx, qw, sw, ops.SB_BLOCK_128x128, torch.bfloat16, c=c)
+        fn = lambda: ops.blockscaled_gemm(qx, sx, qw, sw, ops.SB_BLOCK_128x128, torch.bfloat16, c=c, workspace=ws)
         work = {"flops": GEMM_FLOPS}
     elif case == "wgrad":
         wg = inputs.wgrad(dev)
         a, sa = ops.quant_act_1x128(wg.dy, transposed=True)
         b, sb = ops.quant_act_1x128(wg.x, transposed=True)
         del wg
-        fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_ROW_1x128, torch.float32)
+        cw = torch.empty((2048, 7168), dtype=torch.float32, device=dev)
+        fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_ROW_1x128, torch.float32, c=cw, workspace=ws)
         work = {"flops": 2.0 * 2048 * 7168 * 4096}
     elif case == "gemm_e4m3":
         d = inputs.dense(dev)
@@ -800,7 +852,7 @@ def run_case(args):
         _, _, b, sb = ops.quant_w_128x128_dual(dg.w)
         del dg
         c = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
-        fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_BLOCK_128x128, torch.bfloat16, c=c)
+        fn = lambda: ops.blockscaled_gemm(a, sa, b, sb, ops.SB_BLOCK_128x128, torch.bfloat16, c=c, workspace=ws)
         work = {"flops": 2.0 * 4096 * 7168 * 18432}
     elif case == "grouped":
         m = inputs.moe(dev, tokens=1024, experts=64)
@@ -819,7 +871,7 @@ def run_case(args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     t = timed(fn, stream, args.iters, 3, flush)
     ops.sync_status()
-    out = {"case": case, "iters": args.iters, "ms": round(t, 4)}
+    out = {"case": case, "stream_k": bool(args.sk), "iters": args.iters, "ms": round(t, 4)}
     if "bytes" in work:
         out["GBps"] = round(work["bytes"] / t / 1e6, 1)
     if "flops" in work:
@@ -840,9 +892,10 @@ def main():
     ap.add_argument("--cpu-sample-qrows", type=int, default=4096)
     ap.add_argument("--ref-rows", type=int, default=256)
     ap.add_argument("--ref-wrows", type=int, default=2048)
-    ap.add_argument("--case", choices=["qrow", "qcol", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad", "gemm_e4m3", "qdelayed"],
+    ap.add_argument("--case", choices=["qrow", "qcol", "qcolpair", "qw", "gemm", "wgrad", "grouped", "qdual", "wdual", "dgrad", "gemm_e4m3", "qdelayed"],
                     help="time one kernel on its workload instead of the step (for profiling)")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--sk", action="store_true", help="--case gemm/wgrad/dgrad: the stream-K schedule")
     args = ap.parse_args()
     if args.case:
         run_case(args)

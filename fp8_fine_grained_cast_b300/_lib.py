@@ -38,6 +38,7 @@ _I64 = ctypes.c_int64
 _I = ctypes.c_int
 SIGNATURES = {
     "fp8_quant_act_1x128": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P]),
+    "fp8_quant_act_1x128_transposed_pair": (_I, [_P, _I64, _I64, _P, _P, _P, _I64, _I64, _P, _P, _I64, _P]),
     "fp8_quant_act_delayed": (_I, [_P, _I64, _I64, _I64, _P, _I, _P, _P, _P]),
     "fp8_quant_w_128x128": (_I, [_P, _I64, _I64, _I64, _P, _P, _P]),
     "fp8_quant_act_1x128_dual": (_I, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -96,6 +97,10 @@ def fp8fg_version() -> int:
 
 def fp8_quant_act_1x128(x, M, K, ldx, transposed, q, s, stream):
     return _check(lib().fp8_quant_act_1x128(x, M, K, ldx, transposed, q, s, stream))
+
+
+def fp8_quant_act_1x128_transposed_pair(x0, K0, ldx0, q0, s0, x1, K1, ldx1, q1, s1, M, stream):
+    return _check(lib().fp8_quant_act_1x128_transposed_pair(x0, K0, ldx0, q0, s0, x1, K1, ldx1, q1, s1, M, stream))
 
 
 def fp8_quant_act_delayed(x, M, K, ldx, amax_history, H, q, s, stream):

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8fg.so")
 SOURCES = ["abi.cu", "quant.cu", "gemm.cu", "tensor_map.cu"]
-HEADERS = ["common.cuh", "e4m3.cuh", "internal.h"]
+HEADERS = ["common.cuh", "e4m3.cuh", "gemm_sched.cuh", "internal.h"]
 PUBLIC_HEADER = os.path.join(ROOT, "include", "fp8fg.h")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

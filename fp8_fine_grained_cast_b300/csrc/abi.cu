@@ -164,6 +164,40 @@ int fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, in
   return FP8FG_OK;
 }
 
+int fp8_quant_act_1x128_transposed_pair(const uint16_t* x0, int64_t K0, int64_t ldx0, uint8_t* q0, float* s0,
+                                        const uint16_t* x1, int64_t K1, int64_t ldx1, uint8_t* q1, float* s1,
+                                        int64_t M, fp8fg_stream_t stream) {
+  g_last_error[0] = '\0';
+  const char* name = "fp8_quant_act_1x128_transposed_pair";
+  if (M < 0 || K0 < 0 || K1 < 0) return fail(FP8FG_ERR_ARG, "%s: negative size", name);
+  if (M % 128) return fail(FP8FG_ERR_ARG, "%s: M=%lld is not a multiple of 128", name, (long long)M);
+  if (K0 % 8 || K1 % 8) return fail(FP8FG_ERR_ARG, "%s: K0=%lld and K1=%lld must be multiples of 8", name, (long long)K0, (long long)K1);
+  if ((K0 > 0 && (ldx0 < K0 || ldx0 % 8)) || (K1 > 0 && (ldx1 < K1 || ldx1 % 8))) {
+    return fail(FP8FG_ERR_ARG, "%s: row strides must be >= K and multiples of 8", name);
+  }
+  if (M > kMaxDim || K0 > kMaxDim || K1 > kMaxDim) return fail(FP8FG_ERR_ARG, "%s: dimension too large", name);
+  const bool use0 = M > 0 && K0 > 0, use1 = M > 0 && K1 > 0;
+  if ((use0 && (!x0 || !q0 || !s0)) || (use1 && (!x1 || !q1 || !s1))) return fail(FP8FG_ERR_ARG, "%s: null pointer", name);
+  if ((use0 && (!aligned16(x0) || !aligned16(q0) || !aligned16(s0))) ||
+      (use1 && (!aligned16(x1) || !aligned16(q1) || !aligned16(s1)))) {
+    return fail(FP8FG_ERR_ARG, "%s: pointers must be 16-byte aligned", name);
+  }
+  if (!use0 && !use1) return FP8FG_OK;
+  DeviceInfo dev;
+  if (int rc = current_device(&dev)) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (use0 && use1) {
+    err = fp8fg::launch_quant_act_cols_pair(x0, K0, ldx0, q0, s0, x1, K1, ldx1, q1, s1, M, st, dev.sm_count);
+  } else if (use0) {
+    err = fp8fg::launch_quant_act_cols(x0, M, K0, ldx0, q0, s0, st, dev.sm_count);
+  } else {
+    err = fp8fg::launch_quant_act_cols(x1, M, K1, ldx1, q1, s1, st, dev.sm_count);
+  }
+  if (err != cudaSuccess) return cuda_fail(err, "fp8_quant_act_1x128_transposed_pair launch");
+  return FP8FG_OK;
+}
+
 int fp8_quant_act_delayed(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* amax_history, int H,
                           uint8_t* q, float* s, fp8fg_stream_t stream) {
   g_last_error[0] = '\0';

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "e4m3.cuh"
+#include "gemm_sched.cuh"
 #include "internal.h"
 
 namespace fp8fg {
@@ -114,122 +115,6 @@ struct GemmCfg : WarpLayout<BN> {
   static_assert(L::kCols % kBoxCols == 0, "epilogue boxes");
 };
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// G consecutive floats (16-, 8- or 4-byte aligned) or zeros.
-template <int G>
-struct Vec;
-template <>
-struct Vec<1> {
-  float v[1];
-  __device__ __forceinline__ void load(const float* p, bool ok) { v[0] = ok ? __ldg(p) : 0.0f; }
-};
-template <>
-struct Vec<2> {
-  float v[2];
-  __device__ __forceinline__ void load(const float* p, bool ok) {
-    const float2 t = ok ? __ldg(reinterpret_cast<const float2*>(p)) : make_float2(0.0f, 0.0f);
-    v[0] = t.x;
-    v[1] = t.y;
-  }
-};
-template <>
-struct Vec<4> {
-  float v[4];
-  __device__ __forceinline__ void load(const float* p, bool ok) {
-    const float4 t = ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    v[0] = t.x;
-    v[1] = t.y;
-    v[2] = t.z;
-    v[3] = t.w;
-  }
-};
-
-// Work schedule of a launch. Data-parallel: CTA c takes tiles c, c + G, ... (G = grid
-// size). Stream-K (sk_tiles > 0): the first dp_tiles tiles (a multiple of G) go data-
-// parallel, and the chunks of the last sk_tiles tiles (G <= sk_tiles < 2G) are divided
-// into G contiguous ranges of whole loader groups (grp chunks), one per CTA, in (tile,
-// chunk) order. A range is at least one tile long, so a tile is cut at most once: the
-// CTA whose range ends inside it computes its head and leaves the FP32 partial sums in
-// workspace slot c with a release flag; the next CTA, whose range starts there, computes
-// the tail last, starting its accumulators from that partial. The chunk order of every
-// element is unchanged, so the result is bit-identical to the data-parallel schedule.
-struct Schedule {
-  int dp_tiles;       // tiles scheduled data-parallel (all of them when sk_tiles == 0)
-  int sk_tiles;       // tiles in the stream-K region, 0 for none
-  int grp;            // chunks per loader group; range boundaries are multiples of it
-  int64_t sk_groups;  // sk_tiles * KB / grp
-};
-
-enum UnitKind { kWhole = 0, kHead = 1, kTail = 2 };
-
-struct Unit {
-  int tile, kb0, kb1, kind;
-};
-
-// The units of this CTA (c = blockIdx.x of G = gridDim.x), in processing order: its head
-// piece (so that the partial is ready early), whole stream-K tiles, data-parallel
-// tiles, its tail piece (last, so that the previous CTA's partial has long been
-// written). One thread derives the description once into shared memory; the roles read
-// it there, so that none keeps it (or the 64-bit arithmetic behind it) in registers.
-struct WorkDesc {
-  int n_units, n_head, head_tile, head_kb1, n_whole, whole0, n_dp, tail_tile, tail_kb0;
-};
-
-__device__ __forceinline__ void work_desc_init(const Schedule& s, int num_tiles, int KB, WorkDesc* wd) {
-  const int c = blockIdx.x, G = gridDim.x;
-  WorkDesc d{};
-  if (s.sk_tiles == 0) {
-    d.n_dp = c < num_tiles ? (num_tiles - 1 - c) / G + 1 : 0;
-  } else {
-    const int64_t g0 = (static_cast<int64_t>(c) * s.sk_groups) / G * s.grp;
-    const int64_t g1 = (static_cast<int64_t>(c + 1) * s.sk_groups) / G * s.grp;
-    d.n_head = (g1 % KB) != 0;
-    d.head_tile = s.dp_tiles + static_cast<int>(g1 / KB);
-    d.head_kb1 = static_cast<int>(g1 % KB);
-    d.whole0 = s.dp_tiles + static_cast<int>((g0 + KB - 1) / KB);
-    d.n_whole = s.dp_tiles + static_cast<int>(g1 / KB) - d.whole0;
-    d.n_dp = s.dp_tiles / G;
-    d.tail_tile = s.dp_tiles + static_cast<int>(g0 / KB);
-    d.tail_kb0 = static_cast<int>(g0 % KB);
-    d.n_units = (g0 % KB) != 0;  // the tail, counted below
-  }
-  d.n_units += d.n_head + d.n_whole + d.n_dp;
-  *wd = d;
-}
-
-template <bool SK>
-__device__ __forceinline__ Unit unit_get(const WorkDesc* wd, int KB, int u) {
-  if constexpr (!SK) return {static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x), 0, KB, kWhole};
-  if (u < wd->n_head) return {wd->head_tile, 0, wd->head_kb1, kHead};
-  u -= wd->n_head;
-  if (u < wd->n_whole) return {wd->whole0 + u, 0, KB, kWhole};
-  u -= wd->n_whole;
-  if (u < wd->n_dp) return {static_cast<int>(blockIdx.x) + u * static_cast<int>(gridDim.x), 0, KB, kWhole};
-  return {wd->tail_tile, wd->tail_kb0, KB, kTail};
-}
-
-// Bounded wait until a flag that another CTA sets with release semantics holds this
-// launch's epoch; the same limit and abort protocol as the mbarrier waits. A value left
-// by an earlier launch that gave up before its tail read it (another epoch) is ignored.
-__device__ __forceinline__ bool flag_wait(const int* flag, int epoch, volatile int* abort_flag) {
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v == epoch) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      record_status(kStatusTimeout);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
 // Scale-loader loop of loader warp `li` (0 or 1): groups of G chunks, alternate groups
 // per warp; slot of chunk c is c % kSlots (kSlots >= 2 G). Requires KB % G == 0 and unit
 // boundaries at multiples of G, so that a group never straddles two units.
@@ -244,7 +129,7 @@ __device__ __forceinline__ void load_scales_impl(int li, int lane, int KB, int M
   uint32_t it = 0;
   const int n_units = wd->n_units;
   for (int u = 0; u < n_units; ++u) {
-    const Unit w = unit_get<SK>(wd, KB, u);
+    const Unit w = unit_get<SK>(wd, KB, u, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
     int m_blk, n_blk, e;
     tile_coords(w.tile, m_blk, n_blk, e);
     const int m0 = m_blk * kBM;
@@ -295,7 +180,8 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                             void* __restrict__ c_out, float* __restrict__ c_scale, const float* __restrict__ sa,
                             const float* __restrict__ sb, const int32_t* __restrict__ offsets, int E, int M, int N,
-                            int K, int num_m_tiles, int num_n_tiles, const __grid_constant__ Schedule sched,
+                            int K, int num_m_tiles, int num_n_tiles, int m_group,
+                            const __grid_constant__ Schedule sched,
                             float* __restrict__ ws_partial, int* __restrict__ ws_flags, int sk_epoch) {
   using Cfg = GemmCfg<BN, STAGES, SB_KIND, OUT, GROUPED>;
   constexpr int kSlots = Cfg::kSlots;
@@ -343,7 +229,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(head_written, kPromoWarps * 32);
     mbar_init(tail_read, kPromoWarps * 32);
-    work_desc_init(sched, num_tiles, KB, wd);
+    work_desc_init(sched, num_tiles, KB, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), wd);
     *abort_flag = 0;
     *bad_args = (smem_u32(smem) & 1023u) != 0;
     fence_barrier_init();
@@ -398,8 +284,11 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const bool run = !*bad_args;
 
-  // tile t -> (m block, n block, expert). Dense: m fastest, so that the CTAs working at
-  // the same time share B tiles (and A, which fits in L2). Grouped: n fastest, so that
+  // tile t -> (m block, n block, expert). Dense: groups of m_group row blocks, the rows of
+  // a group fastest, so that the CTAs working at the same time share B tiles and the
+  // group's band of A (m_group x 128 rows x K bytes, kept within about 40 MB by the host)
+  // stays in L2 while the group's column tiles stream past; when all of A fits in that
+  // budget the group is all of M (m fastest). Grouped: n fastest, so that
   // consecutive tiles share an expert's rows and concurrent tiles share its weights; the
   // row tiles themselves alternate between the largest and the smallest experts, so that
   // weight streaming (small experts) and tensor work (large experts reusing their weights
@@ -418,8 +307,13 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       e = s_sorted[lo];
       m_blk = s_off[e] / kBM + (a - s_cum[lo]);
     } else {
-      m_blk = t % num_m_tiles;
-      n_blk = t / num_m_tiles;
+      const int span = m_group * num_n_tiles;
+      const int grp = t / span;
+      const int in = t - grp * span;
+      const int m_first = grp * m_group;
+      const int gm = min(m_group, num_m_tiles - m_first);
+      m_blk = m_first + in % gm;
+      n_blk = in / gm;
       e = 0;
     }
   };
@@ -434,7 +328,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int u = 0; ok && u < wd->n_units; ++u) {
-          const Unit w = unit_get<SK>(wd, KB, u);
+          const Unit w = unit_get<SK>(wd, KB, u, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
           int m_blk, n_blk, e;
           tile_coords(w.tile, m_blk, n_blk, e);
           const int a_row = m_blk * kBM;
@@ -464,7 +358,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         uint32_t it = 0;
         bool ok = true;
         for (int u = 0; ok && u < wd->n_units; ++u) {
-          const Unit w = unit_get<SK>(wd, KB, u);
+          const Unit w = unit_get<SK>(wd, KB, u, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t st = it % STAGES;
             const uint32_t buf = it % kNumAcc;
@@ -522,7 +416,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int u = 0; ok && u < wd->n_units; ++u) {
-        const Unit w = unit_get<SK>(wd, KB, u);
+        const Unit w = unit_get<SK>(wd, KB, u, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x));
         int m_blk, n_blk, e;
         tile_coords(w.tile, m_blk, n_blk, e);
         const int m0 = m_blk * kBM;
@@ -541,7 +435,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
           // then clears the flag, after all have read. Each CTA has at most one tail
           // unit, so the barrier completes at most once (phase 0). (Loading the partial
           // into the accumulators directly made the compiler spill them.)
-          ok = flag_wait(ws_flags + blockIdx.x - 1, sk_epoch, abort_flag);
+          ok = flag_wait(ws_flags + blockIdx.x - 1, sk_epoch, abort_flag, &g_gemm_status);
           if (ok) {
             const float4* src = reinterpret_cast<const float4*>(
                 ws_partial + (static_cast<size_t>(blockIdx.x - 1) * kBM + row) * BN + g * kCols);
@@ -742,17 +636,6 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-// Epoch of a stream-K launch: a head CTA releases its partial sums by writing the epoch
-// into its flag, the tail CTA waits for exactly that value and then clears the flag.
-// Distinct launches get distinct epochs (1 .. 2^31 - 1, cycling), so a flag left set
-// by a launch whose tail gave up (a bounded wait that ran out) cannot release a later
-// launch's tail early.
-std::atomic<uint32_t> g_streamk_epoch{0};
-
-int next_streamk_epoch() {
-  return static_cast<int>(g_streamk_epoch.fetch_add(1, std::memory_order_relaxed) % 0x7FFFFFFFu) + 1;
-}
-
 // Stream-K workspace: one FP32 partial tile (128 x 256) per CTA, then one flag per CTA.
 constexpr size_t kPartialTileBytes = static_cast<size_t>(kBM) * 256 * 4;
 size_t gemm_partial_bytes(int ctas) { return static_cast<size_t>(ctas) * kPartialTileBytes; }
@@ -781,6 +664,9 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 
   const int num_m = static_cast<int>((M + kBM - 1) / kBM);
   const int num_n = static_cast<int>((N + BN - 1) / BN);
+  // dense raster: row-block groups whose band of A stays within about 40 MB of L2
+  const int64_t band = (int64_t(40) << 20) / (kBM * K);
+  const int m_group = static_cast<int>(band < 1 ? 1 : band > num_m ? num_m : band);
   const int64_t tiles = static_cast<int64_t>(num_m) * num_n;
   const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
   Schedule sched{static_cast<int>(tiles), 0, 1, 0};
@@ -800,7 +686,7 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
     epoch = next_streamk_epoch();
   }
   kernel<<<grid, Cfg::kThreads, smem, stream>>>(tmA, tmB, c, c_scale, sa, sb, offsets, E, static_cast<int>(M),
-                                           static_cast<int>(N), static_cast<int>(K), num_m, num_n, sched,
+                                           static_cast<int>(N), static_cast<int>(K), num_m, num_n, m_group, sched,
                                            ws_partial, ws_flags, epoch);
   err = cudaGetLastError();
   if (err != cudaSuccess) return {err, "kernel launch"};
@@ -808,6 +694,19 @@ LaunchResult run_gemm(const uint8_t* qa, const float* sa, const uint8_t* qb, con
 }
 
 }  // namespace
+
+// Epoch of a stream-K launch: a head CTA releases its partial sums by writing the epoch
+// into its flag, the tail CTA waits for exactly that value and then clears the flag.
+// Distinct launches get distinct epochs (1 .. 2^31 - 1, cycling), so a flag left set
+// by a launch whose tail gave up (a bounded wait that ran out) cannot release a later
+// launch's tail early.
+namespace {
+std::atomic<uint32_t> g_streamk_epoch{0};
+}  // namespace
+
+int next_streamk_epoch() {
+  return static_cast<int>(g_streamk_epoch.fetch_add(1, std::memory_order_relaxed) % 0x7FFFFFFFu) + 1;
+}
 
 // Library-owned stream-K workspace for fp8_blockscaled_gemm_sk_static: room for the
 // partial tiles and flags of a device with up to kStaticScratchSms SMs (about 20 MB). One
@@ -830,10 +729,10 @@ LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const u
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
                                      int64_t K, cudaStream_t stream, int sm_count, void* workspace) {
   // 128 x 256 tiles throughout: 128-column tiles (with two or with four TMEM
-  // accumulators), tried for the weight-gradient shape whose 256-column tiles leave a
-  // nearly empty last wave, measured slower on every workload. The stream-K variants
-  // (with a workspace) are separate instantiations, so that the data-parallel kernel
-  // carries none of their code.
+  // accumulators, on one CTA or on a CTA pair with cta_group::2 MMAs), tried for the
+  // weight-gradient shape whose 256-column tiles leave a nearly empty last wave, measured
+  // slower on every workload. The stream-K variants (with a workspace) are separate
+  // instantiations, so that the data-parallel kernel carries none of their code.
   const bool sk = workspace != nullptr;
   if (sb_kind == 0) {
     if (c_kind == 2) return run_gemm<256, 4, 0, 2, false>(qa, sa, qb, sb, nullptr, 0, M, N, K, N, c, c_scale, stream, sm_count);

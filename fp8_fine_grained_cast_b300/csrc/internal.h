@@ -12,6 +12,11 @@ cudaError_t launch_quant_act_rows(const uint16_t* x, int64_t M, int64_t K, int64
                                   cudaStream_t stream, int sm_count);
 cudaError_t launch_quant_act_cols(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
                                   cudaStream_t stream, int sm_count);
+// Tiles along M for two tensors with the same M in one launch: x0 [M][K0] -> q0[K0][M],
+// s0[K0][M/128] and x1 [M][K1] -> q1[K1][M], s1[K1][M/128]; M % 128 == 0.
+cudaError_t launch_quant_act_cols_pair(const uint16_t* x0, int64_t K0, int64_t ldx0, uint8_t* q0, float* s0,
+                                       const uint16_t* x1, int64_t K1, int64_t ldx1, uint8_t* q1, float* s1,
+                                       int64_t M, cudaStream_t stream, int sm_count);
 // Both orientations from one read: q[M][K], s[M][K/128] (tiles along K) and
 // qt[K][M], st[K][M/128] (tiles along M); M and K multiples of 128.
 cudaError_t launch_quant_act_dual(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, float* s,
@@ -51,6 +56,8 @@ LaunchResult launch_blockscaled_gemm(const uint8_t* qa, const float* sa, const u
                                      int sb_kind, void* c, float* c_scale, int c_kind, int64_t M, int64_t N,
                                      int64_t K, cudaStream_t stream, int sm_count, void* workspace = nullptr);
 size_t gemm_workspace_bytes(int sm_count);
+// Epoch of a stream-K launch (1 .. 2^31 - 1, cycling; distinct for consecutive launches).
+int next_streamk_epoch();
 // Address (current device) and size of the library-owned static stream-K workspace.
 cudaError_t gemm_static_scratch(void** ptr, size_t* bytes);
 

@@ -77,6 +77,31 @@ def quant_act_1x128(x: torch.Tensor, transposed: bool = False, q=None, s=None):
     return q, s
 
 
+def quant_act_1x128_transposed_pair(x0: torch.Tensor, x1: torch.Tensor, out=None):
+    """Tiles along M of two bf16 tensors with the same M ([M, K0] and [M, K1]) in one
+    launch: returns (q0 [K0, M], s0 [K0, M/128], q1 [K1, M], s1 [K1, M/128]), the results of
+    quant_act_1x128(x0, transposed=True) and quant_act_1x128(x1, transposed=True)."""
+    for t, n in ((x0, "x0"), (x1, "x1")):
+        _need(t, torch.bfloat16, n, 2)
+        _rows_contiguous(t, n)
+    if x0.device != x1.device:
+        raise ValueError("x0 and x1 must be on the same device")
+    M, K0 = x0.shape
+    if x1.shape[0] != M:
+        raise ValueError("x0 and x1 must have the same number of rows")
+    K1 = x1.shape[1]
+    q0, s0, q1, s1 = (None,) * 4 if out is None else out
+    dev = x0.device
+    q0 = _out_or_new(q0, (K0, M), torch.uint8, dev, "q0")
+    s0 = _out_or_new(s0, (K0, M // 128), torch.float32, dev, "s0")
+    q1 = _out_or_new(q1, (K1, M), torch.uint8, dev, "q1")
+    s1 = _out_or_new(s1, (K1, M // 128), torch.float32, dev, "s1")
+    _lib.fp8_quant_act_1x128_transposed_pair(x0.data_ptr(), K0, x0.stride(0), q0.data_ptr(), s0.data_ptr(),
+                                             x1.data_ptr(), K1, x1.stride(0), q1.data_ptr(), s1.data_ptr(), M,
+                                             _stream())
+    return q0, s0, q1, s1
+
+
 def new_amax_history(H: int, device) -> torch.Tensor:
     """Zero-initialized history state for quant_act_delayed: float32 [H + 1]."""
     return torch.zeros(H + 1, dtype=torch.float32, device=device)

@@ -87,6 +87,24 @@ int fp8_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, in
                         uint8_t *q, float *s, fp8fg_stream_t stream);
 
 /*
+ * The tiles-along-M quantization (fp8_quant_act_1x128 with transposed == 1) of two
+ * tensors that share M, in one launch: typically the two operands of a weight-gradient
+ * GEMM dW = dY^T . X, whose reduction runs over the tokens ("Unified E4M3 format in
+ * DeepSeek-V3": E4M3 with 1x128 tiles in the backward pass as well). One launch instead
+ * of two saves a launch's fixed cost and spreads the blocks of both tensors over all SMs.
+ *
+ * x0: bf16 [M][K0], row stride ldx0 >= K0; x1: bf16 [M][K1], row stride ldx1 >= K1
+ * (strides and K0, K1 multiples of 8; M % 128 == 0).
+ * Outputs, bit-identical to two calls of fp8_quant_act_1x128(.., transposed = 1, ..):
+ *     q0[K0][M], s0[K0][M/128] and q1[K1][M], s1[K1][M/128].
+ * A tensor with K = 0 is skipped (its pointers and row stride are not used).
+ * Returns FP8FG_ERR_ARG for a null pointer, misalignment or a shape rule broken.
+ */
+int fp8_quant_act_1x128_transposed_pair(const uint16_t *x0, int64_t K0, int64_t ldx0, uint8_t *q0, float *s0,
+                                        const uint16_t *x1, int64_t K1, int64_t ldx1, uint8_t *q1, float *s1,
+                                        int64_t M, fp8fg_stream_t stream);
+
+/*
  * Delayed (history-based) quantization, the contrast to the online scaling above
  * ("Online quantization vs delayed quantization in DeepSeek-V3", items 2-3: delayed
  * quantization derives the scale from maximum values recorded in earlier iterations

@@ -195,3 +195,24 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         _lib.lib()
     assert isinstance(ctypes.CDLL, type)
+
+
+def test_quant_transposed_pair_argument_errors(lib):
+    f = lib.fp8_quant_act_1x128_transposed_pair
+    ok = [FAKE, 256, 256, FAKE, FAKE, FAKE, 512, 512, FAKE, FAKE, 384, None]
+
+    def with_(**kw):
+        names = ["x0", "K0", "ldx0", "q0", "s0", "x1", "K1", "ldx1", "q1", "s1", "M", "stream"]
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return _rc(f, *a)
+    assert with_(M=100) == _lib.FP8FG_ERR_ARG                                   # M % 128
+    assert b"multiple of 128" in lib.fp8fg_last_error()
+    assert with_(K1=12) == _lib.FP8FG_ERR_ARG                                   # K % 8
+    assert with_(ldx0=128) == _lib.FP8FG_ERR_ARG                                # ldx < K
+    assert with_(x1=None) == _lib.FP8FG_ERR_ARG                                 # null
+    assert with_(q0=FAKE + 8) == _lib.FP8FG_ERR_ARG                             # misaligned
+    assert with_(K0=-1) == _lib.FP8FG_ERR_ARG                                   # negative
+    assert with_(M=0, x0=None, x1=None, q0=None, q1=None, s0=None, s1=None) == _lib.FP8FG_OK   # empty
+    assert lib.fp8fg_last_error() == b""

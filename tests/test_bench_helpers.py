@@ -40,3 +40,20 @@ def test_rescale_touches_only_tensor_rows():
     assert rows["g"]["frac"] == 0.25 and rows["g"]["stream_k"]["frac"] == 0.375
     assert rows["q"]["frac"] == 0.8
     assert rows["floor"] == {"events_only": 1.2}
+
+
+def test_oracle_threads_split_rows_and_limit_blas():
+    """The CPU baseline divides the oracle's quantizer over row blocks (boundaries on
+    whole 128-row blocks, results concatenated in order) and limits BLAS to the thread
+    count it reports."""
+    import numpy as np
+    from oracle import fp8_oracle as O
+    x = np.random.default_rng(0).standard_normal((640, 256)).astype(np.float32)
+    with bench.OracleThreads(3) as th:
+        q, s = th.rows(O.quant_act_1x128, x)
+        w = th.rows(O.quant_w_128x128, x)
+        assert th.blas_threads in (None, 3)
+    rq, rs = O.quant_act_1x128(x)
+    wq, ws = O.quant_w_128x128(x)
+    assert np.array_equal(q, rq) and np.array_equal(s, rs)
+    assert np.array_equal(w[0], wq) and np.array_equal(w[1], ws)

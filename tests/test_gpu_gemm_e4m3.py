@@ -24,8 +24,9 @@ from tests.test_gpu_gemm import dev, f32, random_quantized
 pytestmark = pytest.mark.gpu
 
 # Codes of the full dense test (98 sampled rows x 18432 columns = 1.8M codes) that may
-# differ from the oracle by one step next to a rounding midpoint.
-DENSE_FULL_MAX_DIFFERING = 2000
+# differ from the oracle by one step next to a rounding midpoint: 7 were observed on a
+# B300, the cap is about twice that.
+DENSE_FULL_MAX_DIFFERING = 16
 
 
 def run(qa, sa, qb, sb, sb_kind, device):

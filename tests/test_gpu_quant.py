@@ -187,3 +187,36 @@ def test_transposed_many_blocks_and_ragged_columns(cuda_device):
         xd = bf16_dev(x, cuda_device)
         q, s = ops.quant_act_1x128(xd, transposed=True)
         assert_same_quant(q, s, *O.quant_act_1x128_transposed(f32(xd)))
+
+
+def test_transposed_pair_wgrad_operands(cuda_device):
+    """Both weight-gradient operands (dY [4096, 2048], X [4096, 7168]) in one launch:
+    bit-identical to two single calls, which the oracle pins at full size above; and a
+    ragged second tensor (K = 264, padded row stride) against the oracle directly."""
+    w = inputs.wgrad(cuda_device)
+    q0, s0, q1, s1 = ops.quant_act_1x128_transposed_pair(w.dy, w.x)
+    r0 = ops.quant_act_1x128(w.dy, transposed=True)
+    r1 = ops.quant_act_1x128(w.x, transposed=True)
+    ops.sync_status()
+    assert torch.equal(q0, r0[0]) and torch.equal(s0.view(torch.int32), r0[1].view(torch.int32))
+    assert torch.equal(q1, r1[0]) and torch.equal(s1.view(torch.int32), r1[1].view(torch.int32))
+    rng = np.random.default_rng(41)
+    a = rng.standard_normal((512, 384)).astype(np.float32)
+    b = rng.standard_normal((512, 272)).astype(np.float32) * 3.0
+    b[rng.random(b.shape) < 0.002] *= 60.0
+    b[128:256, 7] = 0.0                                                    # an all-zero tile
+    xa = bf16_dev(a, cuda_device)
+    xb = bf16_dev(b, cuda_device)[:, :264]                                 # row stride 272
+    q0, s0, q1, s1 = ops.quant_act_1x128_transposed_pair(xa, xb)
+    ops.sync_status()
+    assert_same_quant(q0, s0, *O.quant_act_1x128_transposed(f32(xa)))
+    assert_same_quant(q1, s1, *O.quant_act_1x128_transposed(f32(xb)))
+
+
+def test_transposed_pair_with_an_empty_tensor(cuda_device):
+    x = bf16_dev(np.random.default_rng(42).standard_normal((256, 128)).astype(np.float32), cuda_device)
+    e = torch.empty((256, 0), dtype=torch.bfloat16, device=cuda_device)
+    q0, s0, q1, s1 = ops.quant_act_1x128_transposed_pair(e, x)
+    ops.sync_status()
+    assert q0.shape == (0, 256)
+    assert_same_quant(q1, s1, *O.quant_act_1x128_transposed(f32(x)))
