@@ -337,7 +337,10 @@ def run_ours(args, rank, world, local):
                      "act_frac_hbm": round(qx_bytes / (t_qx / 1e3) / 1e9 / hbm_peak, 4),
                      "w_128x128_GBps": round(qw_bytes / (t_qw / 1e3) / 1e9, 1),
                      "w_frac_hbm": round(qw_bytes / (t_qw / 1e3) / 1e9 / hbm_peak, 4),
-                     "hbm_peak_GBps": hbm_peak},
+                     "hbm_peak_GBps": hbm_peak,
+                     "note": ("in-step figures: the X quantizer follows the previous step's GEMM, whose "
+                              "C (151 MB) is still partly dirty in L2 and is written back during it; "
+                              "the quantizers alone are in rows")},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": x.numel() * 2 + w.numel() * 2, "d2h_bytes_per_step": c.numel() * 2,
                 "pipelining": "uploads, kernels and downloads of consecutive steps on three streams"},

@@ -13,15 +13,19 @@
 //   warp 1     TMEM owner and MMA issuer: per chunk, 4 x tcgen05.mma (K = 32 each) into
 //              one of two TMEM accumulators (BN columns each), the first with the
 //              accumulate flag cleared, so that each accumulator holds exactly one
-//              chunk's partial sum P[m][n] = sum_{k in chunk} qa[m][k] qb[n][k].
+//              chunk's partial sum P[m][n] = sum_{k in chunk} qa[m][k] qb[n][k]; one
+//              commit per chunk tells both the producer (stage free) and the
+//              promotion warps (accumulator complete).
 //   warps 2-3  scale loaders: per chunk, the 128 row scales of A and the column (or
 //              column-block) scales of B into a shared-memory ring, alternate groups of
 //              chunks per warp
 //   warps 4-11 promotion and epilogue: two warpgroups; warpgroup g owns columns
 //              [g BN/2, (g+1) BN/2) of the tile and warp (w % 4) owns TMEM lanes (rows)
-//              32 (w % 4) .. +31. Per chunk: tcgen05.ld the partial sums, release the
-//              accumulator to the MMA warp, then C_acc += P * (sa[m][kb] * sb(n, kb)) in
-//              FP32 registers. While they promote chunk kb the tensor cores already
+//              32 (w % 4) .. +31. Per chunk: tcgen05.ld the partial sums in rounds of 32
+//              columns (the next round's load issued before this round's arithmetic),
+//              release the accumulator once the last round has arrived, and
+//              C_acc += P * (sa[m][kb] * sb(n, kb)) in FP32 registers. While they
+//              promote chunk kb the tensor cores already
 //              compute chunk kb+1 into the other accumulator. After the last chunk the
 //              accumulators are rounded to the output type, transposed through a small
 //              swizzled shared-memory buffer per warp and written with coalesced 16-byte
@@ -102,9 +106,9 @@ struct GemmCfg : WarpLayout<BN> {
   static constexpr int kOffStaging = kOffB + STAGES * kStageB;
   static constexpr int kOffRing = kOffStaging + L::kPromoWarps * kStagingPerWarp;
   static constexpr int kOffBar = kOffRing + kSlots * kSlotFloats * 4;
-  // full[STAGES], empty[STAGES], tmem_full[kNumAcc], tmem_empty[kNumAcc],
-  // scale_full[kSlots], scale_empty[kSlots], drain, head_written, tail_read
-  static constexpr int kNumBars = 2 * STAGES + 2 * L::kNumAcc + 2 * kSlots + 3;
+  // full[STAGES], done[STAGES], tmem_empty[kNumAcc], scale_full[kSlots],
+  // scale_empty[kSlots], drain, head_written, tail_read
+  static constexpr int kNumBars = 2 * STAGES + L::kNumAcc + 2 * kSlots + 3;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffWork = kOffMisc + 16;  // WorkDesc of this CTA
   static constexpr int kOffOffsets = kOffWork + 48;
@@ -192,10 +196,11 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBar);
   uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
+  // done[s]: the MMAs of the chunk in stage s have completed, so the stage may be refilled
+  // and that chunk's accumulator read (one commit per chunk serves both)
+  uint64_t* done = bars + STAGES;
   constexpr uint32_t kNumAcc = Cfg::kNumAcc;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = tfull + kNumAcc;
+  uint64_t* tempty = bars + 2 * STAGES;
   uint64_t* sfull = tempty + kNumAcc;
   uint64_t* sempty = sfull + kSlots;
   uint64_t* drain = sempty + kSlots;
@@ -216,12 +221,9 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&done[i], 1);
     }
-    for (uint32_t i = 0; i < kNumAcc; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], kPromoWarps);
-    }
+    for (uint32_t i = 0; i < kNumAcc; ++i) mbar_init(&tempty[i], kPromoWarps);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(&sfull[i], 32);
       mbar_init(&sempty[i], SB_KIND == 0 ? kPromoWarps : kPromoWarps * 32);
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
           const int b_row = (GROUPED ? e * N : 0) + n_blk * BN;
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             const uint32_t st = it % STAGES;
-            if (!mbar_wait(&empty[st], ((it / STAGES) & 1u) ^ 1u, abort_flag)) {
+            if (!mbar_wait(&done[st], ((it / STAGES) & 1u) ^ 1u, abort_flag)) {
               ok = false;
               break;
             }
@@ -376,8 +378,7 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
               // advance 32 bytes (= 32 E4M3 values) along K inside the swizzle atom
               mma_f8f6f4(d, a0 + 2u * k, b0 + 2u * k, idesc, k > 0 ? 1u : 0u);
             }
-            mma_commit(&empty[st]);
-            mma_commit(&tfull[buf]);
+            mma_commit(&done[st]);
             ++it;
           }
         }
@@ -474,62 +475,48 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
             const uint32_t dep = __reduce_or_sync(0xFFFFFFFFu, __float_as_uint(sc));
             if (lane == 0) mbar_arrive_after(&sempty[slot], dep);
           }
-          if (!mbar_wait(&tfull[buf], (it / kNumAcc) & 1u, abort_flag)) {
+          // the chunk's accumulator is complete: its stage's done barrier (the MMA warp
+          // runs at most kNumAcc chunks ahead, fewer than STAGES, so no phase is skipped)
+          if (!mbar_wait(&done[it % STAGES], (it / STAGES) & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t t_col = t_lane + buf * Cfg::kTmemBuf + g * kCols;
-          if constexpr (SB_KIND == 0) {
-            // rounds of 64 columns: two x32 loads, one wait, 32 packed FMAs with the
-            // chunk's scale product sa[m][kb] * sb[n block][kb]
-            const float2 sc2 = make_float2(sc, sc);
+          // rounds of 32 columns with two register buffers: the load of round p + 1 is
+          // issued before the arithmetic of round p, so that its latency overlaps it; the
+          // accumulator goes back to the MMA warp once the last round's load has arrived
+          const float2 sa2 = make_float2(sa_v, sa_v);
+          const float2 sc2 = make_float2(sc, sc);
+          uint32_t wa[32], wb[32];
+          tmem_ld_32x32b_x32(t_col, wa);
 #pragma unroll
-            for (int p = 0; p < kCols / 64; ++p) {
-              uint32_t w0[32], w1[32];
-              tmem_ld_32x32b_x32(t_col + 64 * p, w0);
-              tmem_ld_32x32b_x32(t_col + 64 * p + 32, w1);
-              tmem_wait_ld_tied(w0);
-              tmem_wait_ld_tied(w1);
-              if (p == kCols / 64 - 1) {  // this warp has read its whole chunk slice
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
-              }
-              float2* a = acc2 + 32 * p;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                a[j] = __ffma2_rn(make_float2(__uint_as_float(w0[2 * j]), __uint_as_float(w0[2 * j + 1])), sc2, a[j]);
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                a[16 + j] =
-                    __ffma2_rn(make_float2(__uint_as_float(w1[2 * j]), __uint_as_float(w1[2 * j + 1])), sc2, a[16 + j]);
-              }
+          for (int p = 0; p < kCols / 32; ++p) {
+            uint32_t(&cur)[32] = (p & 1) ? wb : wa;
+            uint32_t(&nxt)[32] = (p & 1) ? wa : wb;
+            tmem_wait_ld_tied(cur);
+            if (p + 1 < kCols / 32) {
+              tmem_ld_32x32b_x32(t_col + 32 * (p + 1), nxt);
+            } else {  // this warp has read its whole chunk slice
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[buf]);
             }
-          } else {
-            // rounds of 32 columns: one x32 load, one wait, per-column scale products
-            // sa[m][kb] * sb[n][kb] and 16 packed FMAs
-            const float2 sa2 = make_float2(sa_v, sa_v);
+            float2* acp = acc2 + 16 * p;
+            if constexpr (SB_KIND == 0) {
 #pragma unroll
-            for (int p = 0; p < kCols / 32; ++p) {
-              uint32_t w[32];
-              tmem_ld_32x32b_x32(t_col + 32 * p, w);
-              tmem_wait_ld_tied(w);
-              if (p == kCols / 32 - 1) {  // this warp has read its whole chunk slice
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
+              for (int j = 0; j < 16; ++j) {
+                acp[j] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), sc2, acp[j]);
               }
-              float2* a = acc2 + 16 * p;
+            } else {
 #pragma unroll
               for (int j = 0; j < 16; j += 2) {
                 const float4 s4 = *reinterpret_cast<const float4*>(sb_s + 32 * p + 2 * j);
                 const float2 t0 = __fmul2_rn(make_float2(s4.x, s4.y), sa2);
                 const float2 t1 = __fmul2_rn(make_float2(s4.z, s4.w), sa2);
-                a[j] = __ffma2_rn(make_float2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1])), t0, a[j]);
-                a[j + 1] =
-                    __ffma2_rn(make_float2(__uint_as_float(w[2 * j + 2]), __uint_as_float(w[2 * j + 3])), t1, a[j + 1]);
+                acp[j] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * j]), __uint_as_float(cur[2 * j + 1])), t0, acp[j]);
+                acp[j + 1] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * j + 2]), __uint_as_float(cur[2 * j + 3])), t1,
+                                        acp[j + 1]);
               }
             }
           }
