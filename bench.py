@@ -76,8 +76,8 @@ def profiled_traffic(kernel: str):
     if not os.path.exists(p):
         return None
     for line in open(p):
-        parts = line.split()
-        if len(parts) == 3 and not line.startswith("#") and parts[0] == kernel:
+        parts = line.split("#", 1)[0].split()          # a trailing comment names the case
+        if len(parts) == 3 and parts[0] == kernel:
             return int(parts[2]) if parts[1] == kernel_source_hash() else None
     return None
 
