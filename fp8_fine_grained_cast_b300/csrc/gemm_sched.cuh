@@ -1,7 +1,6 @@
-// Work schedule shared by the block-scaled GEMM kernels (gemm.cu: one CTA per tile;
-// gemm_pair.cu: a CTA pair per tile): data-parallel tiles, and the stream-K split of a
-// partial last wave with the hand-off of a cut tile's FP32 partial sums. Also small
-// helpers both kernels use (vector scale loads, BF16 packing).
+// Work schedule of the block-scaled GEMM kernels (gemm.cu): data-parallel tiles, and the
+// stream-K split of a partial last wave with the hand-off of a cut tile's FP32 partial
+// sums. Also small helpers of those kernels (vector scale loads, BF16 packing).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -45,7 +44,7 @@ struct Vec<4> {
   }
 };
 
-// Work schedule of a launch over G workers (CTAs, or CTA pairs) c = 0 .. G-1.
+// Work schedule of a launch over G workers (CTAs) c = 0 .. G-1.
 // Data-parallel: worker c takes tiles c, c + G, ... Stream-K (sk_tiles > 0): the first
 // dp_tiles tiles (a multiple of G) go data-parallel, and the chunks of the last sk_tiles
 // tiles (G <= sk_tiles < 2G) are divided into G contiguous ranges of whole loader groups
