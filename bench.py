@@ -209,14 +209,16 @@ def run_ours(args, rank, world, local):
         if ev is not None:
             ev[3].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    ops.sync_status()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # the warm-up steps run after the sampler has started (starting it leaves the GPU
+        # idle for a moment), directly before the timed steps
+        for _ in range(args.warmup):
+            step()
+        ops.sync_status()
+        barrier()
+        torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
             step(evs[i])

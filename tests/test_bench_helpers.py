@@ -57,3 +57,23 @@ def test_oracle_threads_split_rows_and_limit_blas():
     wq, ws = O.quant_w_128x128(x)
     assert np.array_equal(q, rq) and np.array_equal(s, rs)
     assert np.array_equal(w[0], wq) and np.array_equal(w[1], ws)
+
+
+def test_oracle_threads_without_threadpoolctl(monkeypatch):
+    """Where threadpoolctl is missing (as on some hosts), the BLAS thread count is set and
+    read back through OpenBLAS's own exported functions, and restored afterwards."""
+    import builtins
+    real_import = builtins.__import__
+
+    def no_threadpoolctl(name, *args, **kwargs):
+        if name == "threadpoolctl":
+            raise ImportError("hidden for this test")
+        return real_import(name, *args, **kwargs)
+
+    import numpy  # noqa: F401  (the BLAS library must be loaded before it can be found)
+    before = bench._openblas_threads(None)
+    monkeypatch.setattr(builtins, "__import__", no_threadpoolctl)
+    with bench.OracleThreads(2) as th:
+        assert th.blas_threads in (None, 2)
+    monkeypatch.setattr(builtins, "__import__", real_import)
+    assert bench._openblas_threads(None) == before
