@@ -718,8 +718,8 @@ def oracle_sample_step(x_rows, w_rows, threads):
     xh = d.x.float().numpy()
     wh = d.w.float().numpy()
     t0 = time.perf_counter()
-    qx, sx = threads.rows(O.quant_act_1x128, xh)
-    qw, sw = threads.rows(O.quant_w_128x128, wh)
+    qx, sx = threads.rows(O.quant_act_1x128, xh, unit=1)       # 1x128 tiles: any row split
+    qw, sw = threads.rows(O.quant_w_128x128, wh)                # 128x128 blocks: whole row blocks
     c = O.blockscaled_gemm(qx, sx, qw, sw)
     dt = time.perf_counter() - t0
     assert np.isfinite(c).all()
@@ -734,7 +734,7 @@ def oracle_quantize_rate(rows, threads):
     from oracle import fp8_oracle as O
     x = inputs.quant_only("cpu", rows=rows).float().numpy()
     t0 = time.perf_counter()
-    threads.rows(O.quant_act_1x128, x)
+    threads.rows(O.quant_act_1x128, x, unit=1)
     dt = time.perf_counter() - t0
     nb = x.size * 3 + x.size // 128 * 4
     return nb / dt / 1e9, dt

@@ -101,3 +101,25 @@ def test_streamk_ignores_flags_left_by_an_earlier_launch(cuda_device, stale):
     c_sk = ops.blockscaled_gemm(*args, O.SB_BLOCK_128x128, torch.float32, workspace=ws)
     ops.sync_status()
     assert torch.equal(c_sk, c_dp)
+
+
+# Shapes whose 128 x 256 tiles overfill whole waves of 148 CTAs by varying amounts, with
+# chunk counts K / 128 that are odd (one-chunk loader groups), even but not a multiple of
+# the loader group, or small (a head and a tail in the same tile).
+SWEEP = [(19328, 512, 640), (4096, 1536, 896), (2000, 4864, 256), (640, 7936, 1024), (300, 36864, 384),
+         (38000, 256, 128)]
+
+
+@pytest.mark.parametrize("sb_kind", [O.SB_BLOCK_128x128, O.SB_ROW_1x128])
+@pytest.mark.parametrize("M,N,K", SWEEP)
+def test_streamk_shape_sweep_bit_identical(cuda_device, ws, sb_kind, M, N, K):
+    rng = np.random.default_rng(M * 3 + N + K + sb_kind)
+    qa, sa, qb, sb = random_quantized(rng, M, N, K, sb_kind)
+    args = (dev(qa, cuda_device), dev(sa, cuda_device), dev(qb, cuda_device), dev(sb, cuda_device))
+    out_dtype = torch.bfloat16 if (M + K) % 2 else torch.float32
+    c_dp, c_sk = both(*args, sb_kind, out_dtype, ws)
+    assert torch.equal(c_dp, c_sk)
+    rows = np.array(sorted(set(rng.choice(M, 48, replace=False).tolist()) | {0, M - 1}))
+    ref = O.blockscaled_gemm(qa, sa, qb, sb, sb_kind, rows=rows)
+    tol = 1e-4 if out_dtype == torch.float32 else 8e-3
+    assert O.relative_error(f32(c_sk[torch.from_numpy(rows).to(cuda_device)]), ref) <= tol
