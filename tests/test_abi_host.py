@@ -4,6 +4,8 @@ invalid arguments with FP8FG_ERR_ARG before touching the device."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -216,3 +218,17 @@ def test_quant_transposed_pair_argument_errors(lib):
     assert with_(K0=-1) == _lib.FP8FG_ERR_ARG                                   # negative
     assert with_(M=0, x0=None, x1=None, q0=None, q1=None, s0=None, s1=None) == _lib.FP8FG_OK   # empty
     assert lib.fp8fg_last_error() == b""
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_c_program_against_the_header_and_library(lib, tmp_path):
+    """The ABI used from plain C: tests/csrc/abi_host_check.c includes include/fp8fg.h,
+    links libfp8fg.so and checks argument rejection and empty problems (no GPU needed)."""
+    exe = str(tmp_path / "abi_check")
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    src = os.path.join(ROOT, "tests", "csrc", "abi_host_check.c")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-o", exe, src,
+                    "-L", libdir, "-l:libfp8fg.so", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    checks, failures = map(int, r.stdout.split())
+    assert r.returncode == 0 and failures == 0 and checks >= 19, r.stderr
