@@ -47,8 +47,6 @@ int main(void) {
     expect(fp8_quant_act_1x128_dual(x, 100, 256, 256, q, s, q, s, NULL), FP8FG_ERR_ARG, "act dual M % 128",
            "of 128");
 
-    float hist_slot[4];
-    (void)hist_slot;
     expect(fp8_quant_act_delayed(x, 4, 256, 256, s, 0, q, s, NULL), FP8FG_ERR_ARG, "delayed H", "history");
 
     expect(fp8_blockscaled_gemm(q, s, q, s, 2, p, FP8FG_OUT_BF16, 128, 256, 256, NULL), FP8FG_ERR_ARG,
