@@ -414,6 +414,13 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
       const int row = 32 * qd + lane;
       uint8_t* stg = smem + Cfg::kOffStaging + pw * kStagingPerWarp;
       const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(32 * qd) << 16);
+      // Stream-K partial sums of CTA c: float4 i of row r of warpgroup g's columns at
+      // ((c * (BN / kCols) + g) * (kCols / 4) + i) * kBM + r, so that the 32 rows of a warp
+      // move 512 contiguous bytes per instruction (a row-major tile would scatter each
+      // instruction over 32 lines)
+      auto partial_offset = [&](int cta, int grp, int r) -> size_t {
+        return (static_cast<size_t>(cta) * (BN / kCols) + grp) * (kCols / 4) * kBM + r;
+      };
       uint32_t it = 0;
       bool ok = true;
       for (int u = 0; ok && u < wd->n_units; ++u) {
@@ -438,11 +445,10 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
           // into the accumulators directly made the compiler spill them.)
           ok = flag_wait(ws_flags + blockIdx.x - 1, sk_epoch, abort_flag, &g_gemm_status);
           if (ok) {
-            const float4* src = reinterpret_cast<const float4*>(
-                ws_partial + (static_cast<size_t>(blockIdx.x - 1) * kBM + row) * BN + g * kCols);
+            const float4* src = reinterpret_cast<const float4*>(ws_partial) + partial_offset(blockIdx.x - 1, g, row);
 #pragma unroll
             for (int i = 0; i < kCols / 4; ++i) {
-              const float4 v = __ldcg(src + i);
+              const float4 v = __ldcg(src + i * kBM);
               acc2[2 * i].x += v.x;
               acc2[2 * i].y += v.y;
               acc2[2 * i + 1].x += v.z;
@@ -530,19 +536,22 @@ __global__ void __launch_bounds__(WarpLayout<BN>::kThreads, 1)
         if (w.kind == kHead) {
           // the head of a cut tile: leave the partial sums in slot blockIdx.x; once every
           // promotion thread has stored its part (at most one head unit per CTA: phase 0),
-          // one thread releases them to the CTA that computes the tail. A thread that has
-          // given up still arrives, so the waiter never waits for it; no flag is set then.
+          // one thread releases them to the CTA that computes the tail. The arrive (release,
+          // CTA scope) and that thread's wait (acquire, CTA scope) order every thread's
+          // stores before its GPU-scope fence and release store, so only that thread waits
+          // for the stores to become visible and the others go on with their next unit.
+          // A thread that has given up still arrives, so the waiter never waits for it; no
+          // flag is set then.
           if (ok) {
-            float4* dst = reinterpret_cast<float4*>(ws_partial + (static_cast<size_t>(blockIdx.x) * kBM + row) * BN +
-                                                    g * kCols);
+            float4* dst = reinterpret_cast<float4*>(ws_partial) + partial_offset(blockIdx.x, g, row);
 #pragma unroll
             for (int i = 0; i < kCols / 4; ++i) {
-              __stcg(dst + i, make_float4(acc2[2 * i].x, acc2[2 * i].y, acc2[2 * i + 1].x, acc2[2 * i + 1].y));
+              __stcg(dst + i * kBM, make_float4(acc2[2 * i].x, acc2[2 * i].y, acc2[2 * i + 1].x, acc2[2 * i + 1].y));
             }
-            __threadfence();
           }
           mbar_arrive(head_written);
           if (threadIdx.x == kFirstPromoWarp * 32 && ok && mbar_wait(head_written, 0, abort_flag) && !*abort_flag) {
+            __threadfence();
             asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ws_flags + blockIdx.x), "r"(sk_epoch) : "memory");
           }
           if (!ok) break;
