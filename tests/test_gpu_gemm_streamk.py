@@ -3,7 +3,8 @@ bit-identical to the data-parallel fp8_blockscaled_gemm (the chunk order of ever
 is the same), on shapes whose tiles leave a partial last wave (cut tiles, several chunk
 groups per cut, one-chunk groups when K / 128 is not a multiple of the group), on the
 full dgrad and wgrad workloads, over repeated calls on one workspace (the flags are left
-cleared), and within the oracle tolerance; a too small workspace is refused."""
+cleared), over dozens of launches queued back to back on one workspace, and within the
+oracle tolerance; a too small workspace is refused."""
 import numpy as np
 import pytest
 import torch
@@ -123,3 +124,22 @@ def test_streamk_shape_sweep_bit_identical(cuda_device, ws, sb_kind, M, N, K):
     ref = O.blockscaled_gemm(qa, sa, qb, sb, sb_kind, rows=rows)
     tol = 1e-4 if out_dtype == torch.float32 else 8e-3
     assert O.relative_error(f32(c_sk[torch.from_numpy(rows).to(cuda_device)]), ref) <= tol
+
+
+@pytest.mark.parametrize("M,N,K,sb_kind", [(2000, 4864, 256, O.SB_ROW_1x128), (2048, 7168, 4096, O.SB_ROW_1x128),
+                                           (4096, 1536, 896, O.SB_BLOCK_128x128)])
+def test_streamk_back_to_back_launches_stay_bit_identical(cuda_device, ws, M, N, K, sb_kind):
+    # Many launches on one workspace with no host synchronisation in between: every cut
+    # tile's partial sums must be visible to the CTA that finishes the tile in every
+    # launch (one thread per CTA fences before setting the release flag).
+    rng = np.random.default_rng(M + 7 * N + K)
+    qa, sa, qb, sb = random_quantized(rng, M, N, K, sb_kind)
+    args = (dev(qa, cuda_device), dev(sa, cuda_device), dev(qb, cuda_device), dev(sb, cuda_device))
+    c_dp = ops.blockscaled_gemm(*args, sb_kind, torch.float32)
+    outs = [torch.empty_like(c_dp) for _ in range(24)]
+    for rep in range(2):
+        for c in outs:
+            ops.blockscaled_gemm(*args, sb_kind, torch.float32, c=c, workspace=ws)
+        ops.sync_status()
+        bad = [i for i, c in enumerate(outs) if not torch.equal(c, c_dp)]
+        assert not bad, f"launches {bad} of repetition {rep} differ from the data-parallel result"
